@@ -1,0 +1,489 @@
+// Backward kernels (Flash-DMA issue #73: the backward reuses the forward's
+// mask/bias handling and adds the dBias computation; Flash-DMA README, "Key
+// Features": forward and backward share the block skip decisions and dBias
+// is fused into the backward).
+//
+//   bwd_pre_kernel   delta_i = <dO_i, O_i>, lse in log2 units (+inf for rows
+//                    with no kept key and for padding), zero the fp32 dQ
+//                    accumulator.
+//   bwd_kernel       one CTA = (batch, kv head, 128-key tile).  For every
+//                    active query tile (column of the block map) and every
+//                    query head of the GQA group:
+//                      S^T  = K Q^T           (SS, TMEM cols   0..127)
+//                      dP^T = V dO^T          (SS, TMEM cols 128..255)
+//                      P^T  = exp2(S^T*c + bias^T*log2e - lse2)   (mask bits)
+//                      dS^T = P^T (dP^T - delta)
+//                      dV  += P^T dO          (TS: P^T from TMEM)
+//                      dK  += dS^T Q          (SS: dS^T staged in smem)
+//                      dQ   = dS K            (SS, reuses TMEM cols 128..)
+//                    dQ is added to an fp32 accumulator with vector
+//                    reductions; dBias = sum over the group's heads of dS is
+//                    kept in registers (one thread per key) and written once
+//                    per (query tile, key tile); skipped tiles of dBias are
+//                    written as zeros by the same CTA.
+//   dq_convert       fp32 accumulator -> bf16 dQ.
+#include "fdma_internal.h"
+#include "fdma_ptx.cuh"
+
+namespace fdma {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+#define kPosInf (__int_as_float(0x7f800000))
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
+
+// ----------------------------------------------------------------------- preprocess
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;  // (b, i, h), h fastest
+  const int64_t nrows = static_cast<int64_t>(p.B) * p.nqpad * p.Hq;
+  if (row >= nrows) return;
+  const int h = static_cast<int>(row % p.Hq);
+  const int64_t bi = row / p.Hq;
+  const int i = static_cast<int>(bi % p.nqpad);
+  const int b = static_cast<int>(bi / p.nqpad);
+  float acc = 0.f;
+  const bool valid = i < p.Nq;
+  if (valid) {
+    const int64_t off = ((static_cast<int64_t>(b) * p.Nq + i) * p.Hq + h) * p.d;
+    for (int c = lane * 4; c < p.d; c += 128) {
+      const uint2 o = *reinterpret_cast<const uint2*>(p.out + off + c);
+      const uint2 g = *reinterpret_cast<const uint2*>(p.dout + off + c);
+      acc += bf16_to_f32(o.x & 0xFFFFu) * bf16_to_f32(g.x & 0xFFFFu) + bf16_to_f32(o.x >> 16) * bf16_to_f32(g.x >> 16) +
+             bf16_to_f32(o.y & 0xFFFFu) * bf16_to_f32(g.y & 0xFFFFu) + bf16_to_f32(o.y >> 16) * bf16_to_f32(g.y >> 16);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  float* dq = p.dq_acc + row * p.d;
+  for (int c = lane * 4; c < p.d; c += 128) *reinterpret_cast<float4*>(dq + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (lane == 0) {
+    const int64_t o = (static_cast<int64_t>(b) * p.Hq + h) * p.nqpad + i;
+    float l2 = kPosInf;
+    if (valid) {
+      const float l = p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + i];
+      l2 = (l == -kPosInf) ? kPosInf : l * kLog2e;
+    }
+    p.lse2[o] = l2;
+    p.delta[o] = valid ? acc : 0.f;
+  }
+}
+
+__global__ void __launch_bounds__(256) dq_convert_kernel(const DqConvertParams p) {
+  const int64_t idx = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 8;  // element of (b, i, h, d)
+  const int64_t total = static_cast<int64_t>(p.B) * p.Nq * p.Hq * p.d;
+  if (idx >= total) return;
+  const int64_t per_b = static_cast<int64_t>(p.Nq) * p.Hq * p.d;
+  const int64_t b = idx / per_b, rest = idx % per_b;
+  const float* src = p.dq_acc + b * static_cast<int64_t>(p.nqpad) * p.Hq * p.d + rest;
+  const float4 a = *reinterpret_cast<const float4*>(src);
+  const float4 c = *reinterpret_cast<const float4*>(src + 4);
+  *reinterpret_cast<uint4*>(p.dq + idx) =
+      make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(c.x, c.y), pack_bf16x2(c.z, c.w));
+}
+
+// ----------------------------------------------------------------------- main backward
+enum BwdBar : int {
+  kKVFull = 0,
+  kQdoFull = 1,   // +slot
+  kQdoEmpty = 3,  // +slot
+  kSFull = 5,
+  kDpFull = 6,
+  kPReady = 7,
+  kDqFull = 8,
+  kDqFree = 9,
+  kDsFree = 10,
+  kFinal = 11,
+  kDrain = 12,
+  kNumBwdBars = 13
+};
+
+template <int D>
+struct BwdSmem {
+  static constexpr uint32_t kQB = 128u * D * 2u;
+  static constexpr uint32_t kOffK = 0;
+  static constexpr uint32_t kOffV = kQB;
+  static constexpr uint32_t kOffQ = 2 * kQB;    // [2]
+  static constexpr uint32_t kOffDO = 4 * kQB;   // [2]
+  static constexpr uint32_t kOffDS = 6 * kQB;   // 128 keys x 128 queries bf16
+  static constexpr uint32_t kOffLse = kOffDS + 32768;   // [2][128] f32
+  static constexpr uint32_t kOffDelta = kOffLse + 1024; // [2][128] f32
+  static constexpr uint32_t kOffBar = kOffDelta + 1024;
+  static constexpr uint32_t kOffMisc = kOffBar + kNumBwdBars * 8;
+  static constexpr uint32_t kTotal = kOffMisc + 16;
+};
+
+__device__ __forceinline__ uint64_t kmajor_step(int k, uint32_t rows) {
+  return static_cast<uint64_t>(((k >> 2) * rows * 128u + (k & 3) * 32u) >> 4);
+}
+__device__ __forceinline__ uint64_t mnmajor_step(int k) { return static_cast<uint64_t>((k * 2048) >> 4); }
+
+// Iterates the active query tiles of one key-tile column of the block map.
+struct ColIter {
+  const int8_t* col;  // &kmap[(b*Hkv+g)*nTq*nTk + kt]
+  int nTk, nTq;
+  __device__ __forceinline__ int next(int qt) const {
+    do {
+      ++qt;
+    } while (qt < nTq && col[static_cast<int64_t>(qt) * nTk] == kSkip);
+    return qt;
+  }
+};
+
+template <int D, bool HAS_BIAS, bool WANT_DBIAS>
+__global__ void __launch_bounds__(192, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+               const BwdParams p) {
+  using L = BwdSmem<D>;
+  constexpr int KB = D / 64;
+  constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);   // S^T, dP^T
+  constexpr uint32_t IDESC_DV = idesc_bf16(128, D, false, true);     // P^T(tmem) x dO (N contiguous)
+  constexpr uint32_t IDESC_DK = idesc_bf16(128, D, false, true);     // dS^T(K-major) x Q (N contiguous)
+  constexpr uint32_t IDESC_DQ = idesc_bf16(128, D, true, true);      // dS (M contiguous) x K (N contiguous)
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  uint8_t* sK = smem + L::kOffK;
+  uint8_t* sV = smem + L::kOffV;
+  uint8_t* sQ = smem + L::kOffQ;
+  uint8_t* sDO = smem + L::kOffDO;
+  uint8_t* sDS = smem + L::kOffDS;
+  float* sLse = reinterpret_cast<float*>(smem + L::kOffLse);
+  float* sDelta = reinterpret_cast<float*>(smem + L::kOffDelta);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int id = blockIdx.x;
+  const int g = id % p.Hkv;
+  id /= p.Hkv;
+  const int b = id % p.B;
+  const int kt = id / p.B;  // small key tiles (most causal work) first
+  const int k0 = kt * kTile;
+  const int64_t col_base = static_cast<int64_t>(b * p.Hkv + g) * p.nTq * p.nTk + kt;
+  const ColIter it{p.kmap + col_base, p.nTk, p.nTq};
+  const bool ragged_k = (p.Nk & (kTile - 1)) != 0 && kt == p.nTk - 1;
+  const bool ragged_q_any = (p.Nq & (kTile - 1)) != 0;
+
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicCAS(p.err, 0, kDevErrAlign);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumBwdBars; ++i) mbar_init(&bars[i], 1);
+    mbar_init(&bars[kPReady], 128);
+    mbar_init(&bars[kDqFree], 128);
+    misc[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(misc, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = misc[0];
+  const int first_qt = it.next(-1);
+  const bool any_active = first_qt < p.nTq;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && any_active) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+      mbar_arrive_expect_tx(&bars[kKVFull], 2 * L::kQB);
+#pragma unroll
+      for (int c = 0; c < KB; ++c) {
+        tma_load_4d(sK + c * 16384, &tmK, &bars[kKVFull], c * 64, k0, g, b);
+        tma_load_4d(sV + c * 16384, &tmV, &bars[kKVFull], c * 64, k0, g, b);
+      }
+      int n = 0, issued = 0;
+      bool ok = true;
+      for (int qt = first_qt; ok && qt < p.nTq; qt = it.next(qt)) {
+        for (int hh = 0; hh < p.G; ++hh, ++n) {
+          const int h = g * p.G + hh;
+          const int s = n & 1;
+          if (!(ok = mbar_wait(&bars[kQdoEmpty + s], ((n >> 1) & 1) ^ 1, p.err, kDevErrTimeout, abort_flag))) break;
+          mbar_arrive_expect_tx(&bars[kQdoFull + s], 2 * L::kQB + 1024);
+#pragma unroll
+          for (int c = 0; c < KB; ++c) {
+            tma_load_4d(sQ + s * L::kQB + c * 16384, &tmQ, &bars[kQdoFull + s], c * 64, qt * kTile, h, b);
+            tma_load_4d(sDO + s * L::kQB + c * 16384, &tmDO, &bars[kQdoFull + s], c * 64, qt * kTile, h, b);
+          }
+          const int64_t vec = (static_cast<int64_t>(b) * p.Hq + h) * p.nqpad + qt * kTile;
+          bulk_load(sLse + s * 128, p.lse2 + vec, 512, &bars[kQdoFull + s]);
+          bulk_load(sDelta + s * 128, p.delta + vec, 512, &bars[kQdoFull + s]);
+          issued = n + 1;
+        }
+      }
+      if (*abort_flag) {
+        mbar_wait(&bars[kKVFull], 0, p.err, kDevErrTimeout, nullptr);
+        for (int m = issued > 2 ? issued - 2 : 0; m < issued; ++m)
+          mbar_wait(&bars[kQdoFull + (m & 1)], (m >> 1) & 1, p.err, kDevErrTimeout, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && any_active) {
+      bool ok = mbar_wait(&bars[kKVFull], 0, p.err, kDevErrTimeout, abort_flag);
+      tc_fence_after();
+      const uint64_t kdesc_k = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t vdesc_k = sdesc_sw128(smem_u32(sV), 16, 1024);
+      const uint64_t kdesc_mn = sdesc_sw128(smem_u32(sK), 16384, 1024);
+      const uint64_t dsdesc_k = sdesc_sw128(smem_u32(sDS), 16, 1024);
+      const uint64_t dsdesc_mn = sdesc_sw128(smem_u32(sDS), 16384, 1024);
+      int n = 0;
+      for (int qt = first_qt; ok && qt < p.nTq; qt = it.next(qt)) {
+        for (int hh = 0; hh < p.G; ++hh, ++n) {
+          const int s = n & 1;
+          if (!(ok = mbar_wait(&bars[kQdoFull + s], (n >> 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+          tc_fence_after();
+          const uint64_t qdesc_k = sdesc_sw128(smem_u32(sQ + s * L::kQB), 16, 1024);
+          const uint64_t qdesc_mn = sdesc_sw128(smem_u32(sQ + s * L::kQB), 16384, 1024);
+          const uint64_t dodesc_k = sdesc_sw128(smem_u32(sDO + s * L::kQB), 16, 1024);
+          const uint64_t dodesc_mn = sdesc_sw128(smem_u32(sDO + s * L::kQB), 16384, 1024);
+          // S^T = K Q^T
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            umma_ss(tbase, kdesc_k + kmajor_step(k, 128), qdesc_k + kmajor_step(k, 128), IDESC_S, k > 0);
+          umma_commit(&bars[kSFull]);
+          // dP^T = V dO^T into the columns the previous dQ used
+          if (n > 0) {
+            if (!(ok = mbar_wait(&bars[kDqFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            umma_ss(tbase + 128, vdesc_k + kmajor_step(k, 128), dodesc_k + kmajor_step(k, 128), IDESC_S, k > 0);
+          umma_commit(&bars[kDpFull]);
+          if (!(ok = mbar_wait(&bars[kPReady], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
+          tc_fence_after();
+          // dV += P^T dO ; dK += dS^T Q   (K dimension = 128 queries)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            umma_ts(tbase + 256, tbase + k * 8, dodesc_mn + mnmajor_step(k), IDESC_DV, (n > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            umma_ss(tbase + 384, dsdesc_k + kmajor_step(k, 128), qdesc_mn + mnmajor_step(k), IDESC_DK,
+                    (n > 0 || k > 0) ? 1u : 0u);
+          umma_commit(&bars[kQdoEmpty + s]);
+          // dQ = dS K   (K dimension = 128 keys)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            umma_ss(tbase + 128, dsdesc_mn + mnmajor_step(k), kdesc_mn + mnmajor_step(k), IDESC_DQ, k > 0);
+          umma_commit(&bars[kDqFull]);
+          umma_commit(&bars[kDsFree]);
+        }
+      }
+      umma_commit(&bars[kFinal]);
+      umma_commit(&bars[kDrain]);
+      mbar_wait(&bars[kDrain], 0, p.err, kDevErrTimeout, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ compute
+    const int quad = warp & 3;
+    const int j = quad * 32 + lane;  // key row of S^T / dP^T / dK / dV; query row of dQ
+    const int kidx = k0 + j;
+    const bool kin = kidx < p.Nk;
+    const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
+    float acc[WANT_DBIAS ? 128 : 1];
+#pragma unroll
+    for (int c = 0; c < (WANT_DBIAS ? 128 : 1); ++c) acc[c] = 0.f;
+    int n = 0;
+    bool ok = true;
+    for (int qt = first_qt; ok && qt < p.nTq; qt = it.next(qt)) {
+      const int q0 = qt * kTile;
+      const int64_t tile = col_base + static_cast<int64_t>(qt) * p.nTk;
+      const bool partial =
+          p.kmap[tile] == kPartial || ragged_k || (ragged_q_any && qt == p.nTq - 1);
+      uint4 bits = make_uint4(~0u, ~0u, ~0u, ~0u);
+      if (partial) bits = __ldg(&p.bits_col[tile * kTile + j]);
+      const uint32_t bw[4] = {bits.x, bits.y, bits.z, bits.w};
+      const uint16_t* bcol = nullptr;
+      if (HAS_BIAS) bcol = p.bias + b * p.bs_b + g * p.bs_h + static_cast<int64_t>(q0) * p.bs_r + kidx;
+      const int rows_in = min(kTile, p.Nq - q0);
+      for (int hh = 0; hh < p.G; ++hh, ++n) {
+        const int h = g * p.G + hh;
+        const int s = n & 1;
+        if (!(ok = mbar_wait(&bars[kSFull], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        if (!(ok = mbar_wait(&bars[kDpFull], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        if (!(ok = mbar_wait(&bars[kQdoFull + s], (n >> 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        if (n > 0 && !(ok = mbar_wait(&bars[kDsFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        tc_fence_after();
+        const float* lse2 = sLse + s * 128;
+        const float* dlt = sDelta + s * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // 16 queries per chunk
+          uint32_t sr[16], dr[16];
+          tmem_ld16(tl + c * 16, sr);
+          tmem_ld16(tl + 128 + c * 16, dr);
+          float bv[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            bv[e] = 0.f;
+            if (HAS_BIAS && kin && (c * 16 + e) < rows_in)
+              bv[e] = bf16_to_f32(__ldg(bcol + static_cast<int64_t>(c * 16 + e) * p.bs_r));
+          }
+          tmem_ld_wait();
+          uint32_t pk[8], dk[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            float pv[2], dv[2];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const int qi = c * 16 + e + t;
+              const bool keep = (bw[qi >> 5] >> (qi & 31)) & 1u;
+              const float x = fmaf(__uint_as_float(sr[e + t]), p.scale_log2, fmaf(bv[e + t], kLog2e, -lse2[qi]));
+              pv[t] = keep ? ex2(x) : 0.f;
+              dv[t] = pv[t] * (__uint_as_float(dr[e + t]) - dlt[qi]);
+              if (WANT_DBIAS) acc[qi] += dv[t];
+            }
+            pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+            dk[e >> 1] = pack_bf16x2(dv[0], dv[1]);
+          }
+          tmem_st8(tl + c * 8, pk);
+          // dS^T row j, queries c*16..c*16+15: two 16-byte chunks of the SW128 K-major tile
+          uint8_t* rowp = sDS + (c >> 2) * 16384 + j * 128;
+          const int ch0 = (c & 3) * 2;
+          *reinterpret_cast<uint4*>(rowp + (((ch0) ^ (j & 7)) << 4)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
+          *reinterpret_cast<uint4*>(rowp + (((ch0 + 1) ^ (j & 7)) << 4)) = make_uint4(dk[4], dk[5], dk[6], dk[7]);
+        }
+        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[kPReady]);
+        // drain dQ: this thread owns query row q0 + j
+        if (!(ok = mbar_wait(&bars[kDqFull], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        tc_fence_after();
+        float* dqrow = p.dq_acc + ((static_cast<int64_t>(b) * p.nqpad + q0 + j) * p.Hq + h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tl + 128 + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            red_add_v4(dqrow + c * 32 + 4 * v, __uint_as_float(r[4 * v]) * p.scale,
+                       __uint_as_float(r[4 * v + 1]) * p.scale, __uint_as_float(r[4 * v + 2]) * p.scale,
+                       __uint_as_float(r[4 * v + 3]) * p.scale);
+        }
+        tc_fence_before();
+        mbar_arrive(&bars[kDqFree]);
+      }
+      if (WANT_DBIAS && ok) {
+        uint16_t* dcol = p.dbias + (static_cast<int64_t>(b) * p.Hkv + g) * p.Nq * p.Nk +
+                         static_cast<int64_t>(q0) * p.Nk + kidx;
+#pragma unroll
+        for (int qi = 0; qi < 128; ++qi) {
+          if (kin && qi < rows_in) dcol[static_cast<int64_t>(qi) * p.Nk] = static_cast<uint16_t>(pack_bf16x2(acc[qi], 0.f) & 0xFFFFu);
+          acc[qi] = 0.f;
+        }
+      }
+    }
+    // zero-fill dBias tiles of this key column that were skipped
+    if (WANT_DBIAS && ok) {
+      const int cols = min(kTile, p.Nk - k0);
+      for (int qt = 0; qt < p.nTq; ++qt) {
+        if (p.kmap[col_base + static_cast<int64_t>(qt) * p.nTk] != kSkip) continue;
+        const int i = qt * kTile + j;
+        if (i >= p.Nq) continue;
+        uint16_t* drow = p.dbias + ((static_cast<int64_t>(b) * p.Hkv + g) * p.Nq + i) * p.Nk + k0;
+        for (int c = 0; c < cols; c += 8) *reinterpret_cast<uint4*>(drow + c) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    // dK, dV
+    if (ok && n > 0) ok = mbar_wait(&bars[kFinal], 0, p.err, kDevErrTimeout, abort_flag);
+    if (ok) {
+      tc_fence_after();
+      const int64_t off = ((static_cast<int64_t>(b) * p.Nk + kidx) * p.Hkv + g) * D;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        uint16_t* dst = (which == 0 ? p.dk : p.dv) + off;
+        const uint32_t col0 = which == 0 ? 384u : 256u;
+        const float sc = which == 0 ? p.scale : 1.f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          if (n > 0) {
+            tmem_ld32(tl + col0 + c * 32, r);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) r[t] = 0u;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int t = 0; t < 16; ++t)
+            pk[t] = pack_bf16x2(__uint_as_float(r[2 * t]) * sc, __uint_as_float(r[2 * t + 1]) * sc);
+          if (kin) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D, bool HB, bool WD>
+cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                         const BwdParams& p, cudaStream_t stream) {
+  using L = BwdSmem<D>;
+  auto kern = bwd_kernel<D, HB, WD>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(p.nTk) * p.B * p.Hkv;
+  kern<<<grid, 192, L::kTotal, stream>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(p.B) * p.nqpad * p.Hq;
+  bwd_pre_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert(const DqConvertParams& p, cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(p.B) * p.Nq * p.Hq * p.d / 8;
+  if (total == 0) return cudaSuccess;
+  dq_convert_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(int d, bool has_bias, bool want_dbias, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
+  if (d == 128) {
+    if (want_dbias) return launch_bwd_t<128, true, true>(tq, tk, tv, tdo, p, stream);
+    return has_bias ? launch_bwd_t<128, true, false>(tq, tk, tv, tdo, p, stream)
+                    : launch_bwd_t<128, false, false>(tq, tk, tv, tdo, p, stream);
+  }
+  if (d == 64) {
+    if (want_dbias) return launch_bwd_t<64, true, true>(tq, tk, tv, tdo, p, stream);
+    return has_bias ? launch_bwd_t<64, true, false>(tq, tk, tv, tdo, p, stream)
+                    : launch_bwd_t<64, false, false>(tq, tk, tv, tdo, p, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fdma

@@ -1,0 +1,401 @@
+// Forward kernel: tiled attention with dynamic mask and learnable bias
+// (Flash-DMA issue #73, "Project Progress": masked entries become -inf, the
+// scale applies to QK^T, the bias is added, softmax, then P V; Flash-DMA
+// README, "Key Features": blocks whose mask OR is false are skipped with no
+// K/V/bias traffic; FlashMask README, "Sparse computation": element-wise
+// masking only on partially masked blocks).
+//
+// One CTA = one (batch, query head, 128-row query tile).  Six warps:
+//   warp 0      TMA producer: Q once, then K, V and the 128x128 bias tile of
+//               every ACTIVE key tile into two-deep rings (skipped tiles are
+//               never requested);
+//   warp 1      TMEM owner and single-thread tcgen05.mma issuer:
+//               S_n = Q K_n^T (SS, fp32 in TMEM, double-buffered), then
+//               O += P_{n-1} V_{n-1} with P read from TMEM (TS);
+//   warps 2..5  softmax, one thread per query row (TMEM lane): scale, bias,
+//               mask bits on partial tiles, online max/sum with lazy O
+//               rescaling, P written back to TMEM as packed bf16; final
+//               O / l and lse.
+// TMEM columns: S[0] 0..127, S[1] 128..255, O 256..256+d.
+#include "fdma_internal.h"
+#include "fdma_ptx.cuh"
+
+namespace fdma {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8 between rescales
+#define kNegInf (-__int_as_float(0x7f800000))
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+enum FwdBar : int {
+  kQFull = 0,
+  kKFull = 1,    // +slot
+  kKEmpty = 3,   // +slot
+  kVFull = 5,    // +slot
+  kVEmpty = 7,   // +slot
+  kBFull = 9,    // +slot
+  kBEmpty = 11,  // +slot
+  kSFull = 13,   // +slot
+  kPReady = 15,  // +slot
+  kODone = 17,
+  kOFinal = 18,
+  kDrain = 19,
+  kNumFwdBars = 20
+};
+
+template <int D, bool HAS_BIAS>
+struct FwdSmem {
+  static constexpr uint32_t kQB = 128u * D * 2u;  // one Q/K/V tile (bf16)
+  static constexpr uint32_t kBB = 128u * 128u * 2u;
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffK = kQB;
+  static constexpr uint32_t kOffV = kOffK + 2 * kQB;
+  static constexpr uint32_t kOffBias = kOffV + 2 * kQB;
+  static constexpr uint32_t kOffBar = kOffBias + (HAS_BIAS ? 2 * kBB : 0u);
+  static constexpr uint32_t kOffMap = kOffBar + kNumFwdBars * 8;
+  static constexpr uint32_t kOffMisc = kOffMap + kMaxKTiles;
+  static constexpr uint32_t kTotal = kOffMisc + 16;
+};
+
+__device__ __forceinline__ int next_active(const int8_t* row, int kt, int n) {
+  do {
+    ++kt;
+  } while (kt < n && row[kt] == kSkip);
+  return kt;
+}
+
+// Descriptor offset (in the 16-byte units of the start-address field) of the
+// k-th 16-element K step inside a K-major SW128 tile made of 64-column blocks.
+__device__ __forceinline__ uint64_t kmajor_step(int k, uint32_t rows) {
+  return static_cast<uint64_t>(((k >> 2) * rows * 128u + (k & 3) * 32u) >> 4);
+}
+
+template <int D, bool HAS_BIAS>
+__global__ void __launch_bounds__(192, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmB,
+               const FwdParams p) {
+  using L = FwdSmem<D, HAS_BIAS>;
+  constexpr int KB = D / 64;  // 64-column swizzle blocks along the head dim
+  constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
+  constexpr uint32_t IDESC_O = idesc_bf16(128, D, false, true);
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+  int8_t* map_row = reinterpret_cast<int8_t*>(smem + L::kOffMap);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int id = blockIdx.x;
+  const int hh = id % p.G;
+  id /= p.G;
+  const int g = id % p.Hkv;
+  id /= p.Hkv;
+  const int b = id % p.B;
+  id /= p.B;
+  const int qt = p.nTq - 1 - id;  // longest causal rows first
+  const int h = g * p.G + hh;
+  const int q0 = qt * kTile;
+  const int64_t tile_base = (static_cast<int64_t>(b * p.Hkv + g) * p.nTq + qt) * p.nTk;
+  const bool ragged_k = (p.Nk & (kTile - 1)) != 0;
+
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicCAS(p.err, 0, kDevErrAlign);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumFwdBars; ++i) mbar_init(&bars[i], 1);
+    mbar_init(&bars[kBEmpty + 0], 128);
+    mbar_init(&bars[kBEmpty + 1], 128);
+    mbar_init(&bars[kPReady + 0], 128);
+    mbar_init(&bars[kPReady + 1], 128);
+    misc[1] = 0;
+    fence_mbar_init();
+  }
+  for (int kt = threadIdx.x; kt < p.nTk; kt += blockDim.x) map_row[kt] = p.kmap[tile_base + kt];
+  if (warp == 1) {
+    tmem_alloc(misc, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = misc[0];
+  const int first_kt = next_active(map_row, -1, p.nTk);
+  const bool any_active = first_kt < p.nTk;
+
+  uint8_t* sQ = smem + L::kOffQ;
+  uint8_t* sK = smem + L::kOffK;
+  uint8_t* sV = smem + L::kOffV;
+  uint8_t* sB = smem + L::kOffBias;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && any_active) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      if (HAS_BIAS) tma_prefetch_desc(&tmB);
+      mbar_arrive_expect_tx(&bars[kQFull], L::kQB);
+#pragma unroll
+      for (int c = 0; c < KB; ++c) tma_load_4d(sQ + c * 16384, &tmQ, &bars[kQFull], c * 64, q0, h, b);
+      int n = 0;
+      int issued = 0;
+      for (int kt = first_kt; kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
+        const int s = n & 1;
+        const uint32_t ph = ((n >> 1) & 1) ^ 1;
+        const int k0 = kt * kTile;
+        if (!mbar_wait(&bars[kKEmpty + s], ph, p.err, kDevErrTimeout, abort_flag)) break;
+        mbar_arrive_expect_tx(&bars[kKFull + s], L::kQB);
+#pragma unroll
+        for (int c = 0; c < KB; ++c)
+          tma_load_4d(sK + s * L::kQB + c * 16384, &tmK, &bars[kKFull + s], c * 64, k0, g, b);
+        if (HAS_BIAS) {
+          if (!mbar_wait(&bars[kBEmpty + s], ph, p.err, kDevErrTimeout, abort_flag)) break;
+          mbar_arrive_expect_tx(&bars[kBFull + s], L::kBB);
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            tma_load_4d(sB + s * L::kBB + c * 16384, &tmB, &bars[kBFull + s], k0 + c * 64, q0, g, b);
+        }
+        if (!mbar_wait(&bars[kVEmpty + s], ph, p.err, kDevErrTimeout, abort_flag)) break;
+        mbar_arrive_expect_tx(&bars[kVFull + s], L::kQB);
+#pragma unroll
+        for (int c = 0; c < KB; ++c)
+          tma_load_4d(sV + s * L::kQB + c * 16384, &tmV, &bars[kVFull + s], c * 64, k0, g, b);
+        issued = n + 1;
+      }
+      if (*abort_flag) {
+        // let our own copies land before the CTA retires
+        mbar_wait(&bars[kQFull], 0, p.err, kDevErrTimeout, nullptr);
+        for (int m = issued > 2 ? issued - 2 : 0; m < issued; ++m) {
+          const uint32_t ph = (m >> 1) & 1;
+          mbar_wait(&bars[kKFull + (m & 1)], ph, p.err, kDevErrTimeout, nullptr);
+          mbar_wait(&bars[kVFull + (m & 1)], ph, p.err, kDevErrTimeout, nullptr);
+          if (HAS_BIAS) mbar_wait(&bars[kBFull + (m & 1)], ph, p.err, kDevErrTimeout, nullptr);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && any_active) {
+      bool ok = mbar_wait(&bars[kQFull], 0, p.err, kDevErrTimeout, abort_flag);
+      tc_fence_after();
+      const uint64_t qdesc = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      int n = 0;
+      for (int kt = first_kt; ok && kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
+        const int s = n & 1;
+        const uint32_t ph = (n >> 1) & 1;
+        if (!(ok = mbar_wait(&bars[kKFull + s], ph, p.err, kDevErrTimeout, abort_flag))) break;
+        tc_fence_after();
+        const uint64_t kdesc = sdesc_sw128(smem_u32(sK + s * L::kQB), 16, 1024);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          umma_ss(tbase + s * 128, qdesc + kmajor_step(k, 128), kdesc + kmajor_step(k, 128), IDESC_S, k > 0);
+        umma_commit(&bars[kSFull + s]);
+        umma_commit(&bars[kKEmpty + s]);
+        if (n > 0) {
+          const int m = n - 1, sm = m & 1;
+          const uint32_t pm = (m >> 1) & 1;
+          if (!(ok = mbar_wait(&bars[kVFull + sm], pm, p.err, kDevErrTimeout, abort_flag))) break;
+          if (!(ok = mbar_wait(&bars[kPReady + sm], pm, p.err, kDevErrTimeout, abort_flag))) break;
+          tc_fence_after();
+          const uint64_t vdesc = sdesc_sw128(smem_u32(sV + sm * L::kQB), 16384, 1024);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            umma_ts(tbase + 256, tbase + sm * 128 + k * 8, vdesc + static_cast<uint64_t>((k * 2048) >> 4), IDESC_O,
+                    (m > 0 || k > 0) ? 1u : 0u);
+          umma_commit(&bars[kVEmpty + sm]);
+          umma_commit(&bars[kODone]);
+        }
+      }
+      if (ok && n > 0) {
+        const int m = n - 1, sm = m & 1;
+        const uint32_t pm = (m >> 1) & 1;
+        ok = mbar_wait(&bars[kVFull + sm], pm, p.err, kDevErrTimeout, abort_flag) &&
+             mbar_wait(&bars[kPReady + sm], pm, p.err, kDevErrTimeout, abort_flag);
+        if (ok) {
+          tc_fence_after();
+          const uint64_t vdesc = sdesc_sw128(smem_u32(sV + sm * L::kQB), 16384, 1024);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            umma_ts(tbase + 256, tbase + sm * 128 + k * 8, vdesc + static_cast<uint64_t>((k * 2048) >> 4), IDESC_O,
+                    (m > 0 || k > 0) ? 1u : 0u);
+          umma_commit(&bars[kVEmpty + sm]);
+          umma_commit(&bars[kODone]);
+        }
+      }
+      umma_commit(&bars[kOFinal]);
+      umma_commit(&bars[kDrain]);
+      mbar_wait(&bars[kDrain], 0, p.err, kDevErrTimeout, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int i = q0 + r;
+    const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
+    float m_ref = kNegInf, l = 0.f;
+    int n = 0;
+    bool ok = true;
+    uint32_t raw[32];
+    for (int kt = first_kt; kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
+      const int s = n & 1;
+      const uint32_t ph = (n >> 1) & 1;
+      if (!(ok = mbar_wait(&bars[kSFull + s], ph, p.err, kDevErrTimeout, abort_flag))) break;
+      tc_fence_after();
+      const bool partial = map_row[kt] == kPartial || (ragged_k && kt == p.nTk - 1);
+      uint4 bits = make_uint4(~0u, ~0u, ~0u, ~0u);
+      if (partial) bits = __ldg(&p.bits_row[(tile_base + kt) * kTile + r]);
+      float x[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(tl + s * 128 + c * 32, raw);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[c * 32 + j] = __uint_as_float(raw[j]) * p.scale_log2;
+      }
+      if (HAS_BIAS) {
+        if (!(ok = mbar_wait(&bars[kBFull + s], ph, p.err, kDevErrTimeout, abort_flag))) break;
+        const uint8_t* bt = sB + s * L::kBB + r * 128;
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) {
+          const uint4 v = *reinterpret_cast<const uint4*>(bt + (cc >> 3) * 16384 + (((cc & 7) ^ (r & 7)) << 4));
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            x[cc * 8 + 2 * e] = fmaf(__uint_as_float(w[e] << 16), kLog2e, x[cc * 8 + 2 * e]);
+            x[cc * 8 + 2 * e + 1] = fmaf(__uint_as_float(w[e] & 0xFFFF0000u), kLog2e, x[cc * 8 + 2 * e + 1]);
+          }
+        }
+        mbar_arrive(&bars[kBEmpty + s]);
+      }
+      if (partial) {
+        const uint32_t bw[4] = {bits.x, bits.y, bits.z, bits.w};
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (!((bw[c >> 5] >> (c & 31)) & 1u)) x[c] = kNegInf;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+      const float m_new = fmaxf(m_ref, mx);
+      float alpha = 1.f;
+      bool resc = false;
+      if (m_new > m_ref + kRescaleThreshold) {
+        if (m_ref == kNegInf) {
+          m_ref = m_new;
+        } else {
+          alpha = ex2(m_ref - m_new);
+          l *= alpha;
+          m_ref = m_new;
+          resc = true;
+        }
+      }
+      if (__any_sync(0xffffffffu, resc)) {
+        // O holds P_0..P_{n-1} products: wait for PV_{n-1}, then scale this row.
+        if (!(ok = mbar_wait(&bars[kODone], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          tmem_ld32(tl + 256 + c * 32, raw);
+          tmem_ld_wait();
+          uint32_t lo[16], hi[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            lo[j] = __float_as_uint(__uint_as_float(raw[j]) * alpha);
+            hi[j] = __float_as_uint(__uint_as_float(raw[16 + j]) * alpha);
+          }
+          tmem_st16(tl + 256 + c * 32, lo);
+          tmem_st16(tl + 256 + c * 32 + 16, hi);
+        }
+        tmem_st_wait();
+      }
+      const float mu = (m_ref == kNegInf) ? 0.f : m_ref;
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float p0 = ex2(x[c * 32 + 2 * j] - mu);
+          const float p1 = ex2(x[c * 32 + 2 * j + 1] - mu);
+          sum += p0 + p1;
+          pk[j] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tl + s * 128 + c * 16, pk);
+      }
+      l += sum;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars[kPReady + s]);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && n > 0) ok = mbar_wait(&bars[kOFinal], 0, p.err, kDevErrTimeout, abort_flag);
+    if (ok) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint16_t* orow = p.out + ((static_cast<int64_t>(b) * p.Nq + i) * p.Hq + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        if (n > 0) {
+          tmem_ld32(tl + 256 + c * 32, raw);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) raw[j] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          pk[j] = pack_bf16x2(__uint_as_float(raw[2 * j]) * inv, __uint_as_float(raw[2 * j + 1]) * inv);
+        if (i < p.Nq) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+      if (i < p.Nq)
+        p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + i] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : kNegInf;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D, bool HB>
+cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tb,
+                         const FwdParams& p, cudaStream_t stream) {
+  using L = FwdSmem<D, HB>;
+  auto kern = fwd_kernel<D, HB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(p.B) * p.Hq * p.nTq;
+  kern<<<grid, 192, L::kTotal, stream>>>(tq, tk, tv, tb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(int d, bool has_bias, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tb, const FwdParams& p, cudaStream_t stream) {
+  if (d == 128) return has_bias ? launch_fwd_t<128, true>(tq, tk, tv, tb, p, stream)
+                                : launch_fwd_t<128, false>(tq, tk, tv, tb, p, stream);
+  if (d == 64) return has_bias ? launch_fwd_t<64, true>(tq, tk, tv, tb, p, stream)
+                               : launch_fwd_t<64, false>(tq, tk, tv, tb, p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fdma

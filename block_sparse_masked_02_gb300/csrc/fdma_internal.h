@@ -1,0 +1,95 @@
+// Parameter blocks and launcher declarations shared by the host layer
+// (fdma_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fdma.h"
+
+namespace fdma {
+
+constexpr int kTile = 128;           // query rows and key columns per tile
+constexpr int kMaxKTiles = 1024;     // Nk <= 131072
+constexpr int kSkip = 0, kPartial = 1, kFull = 2;
+
+// Device error word values (first writer wins).
+constexpr int kDevErrTimeout = FDMA_ERR_TIMEOUT;
+constexpr int kDevErrAlign = FDMA_ERR_CUDA;
+
+// One 128x128 tile's keep-bits: 128 x 16 bytes.  bits_row[t*128 + r] holds
+// row r (bit c%32 of word c/32 = column c); bits_col[t*128 + c] holds column c
+// (bit r%32 of word r/32 = row r).
+struct ClassifyParams {
+  int B, Nq, Nk, Hkv, nTq, nTk;
+  int mask_kind, causal, no_skip;
+  const uint16_t* mask;
+  int64_t ms_b, ms_h, ms_r;
+  const int32_t* cr;
+  int64_t cr_b, cr_h;
+  int8_t* kmap;      // kernel tile classes (workspace)
+  int8_t* user_map;  // optional caller copy of the true classes
+  uint4* bits_row;
+  uint4* bits_col;
+};
+
+struct FwdParams {
+  int B, Nq, Nk, Hq, Hkv, G, nTq, nTk;
+  float scale_log2;  // scale * log2(e)
+  const int8_t* kmap;
+  const uint4* bits_row;
+  uint16_t* out;  // (B,Nq,Hq,d)
+  float* lse;     // (B,Hq,Nq)
+  int* err;
+};
+
+struct BwdPreParams {
+  int B, Nq, Hq, d, nqpad;
+  const uint16_t* out;
+  const uint16_t* dout;
+  const float* lse;
+  float* lse2;   // (B,Hq,nqpad): lse*log2(e), +inf for empty / padded rows
+  float* delta;  // (B,Hq,nqpad)
+  float* dq_acc; // (B,nqpad,Hq,d), zeroed
+};
+
+struct BwdParams {
+  int B, Nq, Nk, Hq, Hkv, G, nTq, nTk, nqpad;
+  float scale, scale_log2;
+  const int8_t* kmap;
+  const uint4* bits_col;
+  const uint16_t* bias;  // may be null
+  int64_t bs_b, bs_h, bs_r;
+  const float* lse2;
+  const float* delta;
+  float* dq_acc;
+  uint16_t* dk;     // (B,Nk,Hkv,d)
+  uint16_t* dv;     // (B,Nk,Hkv,d)
+  uint16_t* dbias;  // (B,Hkv,Nq,Nk) or null
+  int* err;
+};
+
+struct DqConvertParams {
+  int B, Nq, Hq, d, nqpad;
+  const float* dq_acc;
+  uint16_t* dq;
+};
+
+// Workspace layout (byte offsets, each 256-aligned).
+struct WorkspaceLayout {
+  size_t kmap, bits_row, bits_col, lse2, delta, dq_acc, total_fwd, total_bwd;
+};
+
+WorkspaceLayout workspace_layout(int B, int Nq, int Nk, int Hq, int Hkv, int d);
+
+cudaError_t launch_classify(const ClassifyParams& p, cudaStream_t stream);
+cudaError_t launch_fwd(int d, bool has_bias, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tb, const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream);
+cudaError_t launch_bwd(int d, bool has_bias, bool want_dbias, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_dq_convert(const DqConvertParams& p, cudaStream_t stream);
+
+}  // namespace fdma

@@ -1,0 +1,150 @@
+/*
+ * fdma.h -- C ABI of libfdma: FlashAttention-style tiled attention with a
+ * dynamic 4D mask (dense, or FlashMask column row-ranges), a learnable 4D
+ * bias, block skipping and a fused, GQA-summed dBias, for sm_103a (GB300).
+ *
+ * Operation (Flash-DMA README, "Key Features" and the Quick Start example;
+ * Flash-DMA issue #73, "Project Progress"; FlashMask README, "Formulation"
+ * and "Sparse computation"):
+ *
+ *   keep(b,g,i,j) = mask[b,g,i,j] != 0                          (FDMA_MASK_DENSE)
+ *                 | !(colranges[b,g,j,0] <= i < colranges[b,g,j,1])  (FDMA_MASK_COLRANGES)
+ *                 | 1                                           (FDMA_MASK_NONE)
+ *                   and, with is_causal, j <= i
+ *   S[b,h,i,j]    = scale * <q[b,i,h,:], k[b,j,g,:]> + bias[b,g,i,j]   if keep, else -inf
+ *   O[b,i,h,:]    = sum_j softmax_j(S[b,h,i,:]) v[b,j,g,:]
+ *   lse[b,h,i]    = log sum_j exp(S[b,h,i,j])           (natural log)
+ *
+ * where g = h / (Hq / Hkv) (query heads are grouped contiguously onto kv
+ * heads).  A row with no kept key yields O = 0 and lse = -inf, and receives
+ * and produces zero gradient.  The backward returns dQ, dK, dV and
+ *   dBias[b,g,i,j] = sum_{h in group g} dS[b,h,i,j],  dS = P*(dP - rowsum(dO*O)),
+ * which is exactly 0 wherever keep is false.
+ *
+ * Tiles are 128 (queries) x 128 (keys).  A tile with no kept element is
+ * SKIPPED: its K, V, bias and mask are never loaded by the attention kernels.
+ *
+ * Conventions for every entry point
+ *   - All data pointers are CUDA device pointers owned by the caller; the
+ *     library never allocates, frees or retains them.  `workspace` is
+ *     caller-allocated device memory of at least fdma_workspace_size() bytes.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and keeps no state between calls, except that the
+ *     classification written into the workspace by one call may be reused by
+ *     a later call with the same mask (FDMA_FLAG_REUSE_CLASSIFICATION).
+ *   - Argument errors are reported synchronously as a non-zero fdma_status;
+ *     nothing is launched in that case.  Launch failures return
+ *     FDMA_ERR_CUDA.  Kernel-side time-outs (a wait that exceeded its bound)
+ *     are recorded in a device error word read by fdma_get_device_error().
+ *   - No function throws or aborts.
+ *   - Element types: q, k, v, out, dout, dq, dk, dv, mask, bias, dbias are
+ *     bf16; lse is fp32; colranges is int32.
+ */
+#ifndef FDMA_H_
+#define FDMA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FDMA_API __attribute__((visibility("default")))
+#else
+#define FDMA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FDMA_OK = 0,
+  FDMA_ERR_INVALID = 1,      /* bad argument (shape, pointer, stride, scale) */
+  FDMA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head dim, alignment, causal with Nq != Nk) */
+  FDMA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+  FDMA_ERR_TIMEOUT = 4,      /* a bounded in-kernel wait expired (see fdma_get_device_error) */
+  FDMA_ERR_WORKSPACE = 5     /* workspace missing or smaller than fdma_workspace_size() */
+} fdma_status;
+
+typedef enum { FDMA_MASK_NONE = 0, FDMA_MASK_DENSE = 1, FDMA_MASK_COLRANGES = 2 } fdma_mask_kind;
+
+/* flags */
+#define FDMA_FLAG_REUSE_CLASSIFICATION 1u /* workspace already classified for this mask: skip the classifier */
+#define FDMA_FLAG_NO_SKIP 2u              /* debug: treat every causally allowed tile as PARTIAL (no skipping) */
+
+typedef struct fdma_args {
+  /* problem size: batch, query length, key length, query heads, kv heads, head dim (64 or 128) */
+  int32_t B, Nq, Nk, Hq, Hkv, d;
+
+  /* q (B,Nq,Hq,d), k and v (B,Nk,Hkv,d); strides in ELEMENTS for (batch, seq, head); the
+     head-dim axis is contiguous.  seq/head/batch strides * 2 bytes must be multiples of 16. */
+  const void* q;
+  int64_t q_stride[3];
+  const void* k;
+  int64_t k_stride[3];
+  const void* v;
+  int64_t v_stride[3];
+
+  /* mask selection (fdma_mask_kind) */
+  int32_t mask_kind;
+  /* FDMA_MASK_DENSE: bf16 (B,Hkv,Nq,Nk), nonzero = keep; strides (batch, head, row) in elements,
+     columns contiguous; row stride a multiple of 8 elements, base 16-byte aligned. */
+  const void* mask;
+  int64_t mask_stride[3];
+  /* FDMA_MASK_COLRANGES: int32 (B,Hkv,Nk,2): query rows [start,end) are MASKED for key
+     column j (start >= end: none masked; values outside [0,Nq) are clamped by the test).
+     cr_stride = (batch, head) strides in int32 elements; within one (batch, head) the
+     (Nk, 2) block is contiguous (key j at offset 2*j). */
+  const int32_t* colranges;
+  int64_t cr_stride[2];
+
+  /* optional bf16 bias (B,Hkv,Nq,Nk) (NULL = zero bias); strides (batch, head, row) in
+     elements; row stride a multiple of 8 elements, base 16-byte aligned. */
+  const void* bias;
+  int64_t bias_stride[3];
+
+  int32_t is_causal; /* 1: keep additionally requires j <= i (requires Nq == Nk) */
+  float scale;       /* multiplies Q K^T only; must be finite and > 0 */
+  uint32_t flags;    /* FDMA_FLAG_* */
+
+  void* workspace; /* device memory, >= fdma_workspace_size(args, for_bwd) bytes, 256-byte aligned */
+  size_t workspace_bytes;
+} fdma_args;
+
+/* Bytes of workspace needed by fdma_classify_blocks / fdma_fwd (for_bwd = 0) or by
+   fdma_bwd as well (for_bwd = 1).  Returns 0 when the shape in args is invalid. */
+FDMA_API size_t fdma_workspace_size(const fdma_args* args, int for_bwd);
+
+/* Block classification (Flash-DMA "Key Features": OR-reduction over each
+   mask block; FlashMask "Sparse computation": fully masked / partially masked
+   / unmasked).  Writes the per-tile classes into the workspace and, when
+   block_map != NULL, also to block_map: int8 (B, Hkv, ceil(Nq/128), ceil(Nk/128)),
+   contiguous, values 0 = SKIP (no kept element), 1 = PARTIAL, 2 = FULL (every
+   in-bounds element kept).  Reads the dense mask once; reads no mask above
+   the causal diagonal.  block_m and block_n must be 128. */
+FDMA_API int fdma_classify_blocks(const fdma_args* args, int block_m, int block_n, int8_t* block_map, void* stream);
+
+/* Forward.  Classifies (unless FDMA_FLAG_REUSE_CLASSIFICATION) and computes
+   out: bf16 (B,Nq,Hq,d) contiguous and lse: fp32 (B,Hq,Nq) contiguous. */
+FDMA_API int fdma_fwd(const fdma_args* args, void* out, float* lse, void* stream);
+
+/* Backward.  out, dout: bf16 (B,Nq,Hq,d) contiguous; lse as written by fdma_fwd.
+   Outputs dq: bf16 (B,Nq,Hq,d), dk and dv: bf16 (B,Nk,Hkv,d) (summed over each
+   group's query heads), dbias: bf16 (B,Hkv,Nq,Nk) (NULL: not computed; requires
+   args->bias != NULL), all contiguous.  Every dbias element is written (zeros in
+   skipped tiles and at masked positions).  Classifies unless
+   FDMA_FLAG_REUSE_CLASSIFICATION.  Needs the for_bwd workspace size. */
+FDMA_API int fdma_bwd(const fdma_args* args, const void* out, const void* dout, const float* lse, void* dq, void* dk,
+             void* dv, void* dbias, void* stream);
+
+/* Synchronizes `stream`, returns the first kernel-side error recorded since the last call
+   (FDMA_OK if none) and clears it. */
+FDMA_API int fdma_get_device_error(void* stream);
+
+/* Static, human-readable name of a status code. */
+FDMA_API const char* fdma_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FDMA_H_ */

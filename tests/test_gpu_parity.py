@@ -1,0 +1,229 @@
+"""Element-by-element parity of the sm_103a kernels (through the C ABI) with
+the fp64 oracle on seeded inputs that span several tiles and ragged tails.
+
+Tolerances: block map bit-exact; O max-abs <= 1e-2 and rel-L2 <= 5e-3;
+dQ, dK, dV, dBias rel-L2 <= 1e-2 (bf16 inputs, fp32 accumulation); lse is
+compared to 2e-3 absolute, and rows with no kept key must give lse = -inf and
+O = 0 exactly."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as orc
+from block_sparse_masked_02_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+O_MAXABS, O_RELL2, G_RELL2, LSE_ABS = 1e-2, 5e-3, 1e-2, 2e-3
+
+
+@pytest.fixture(scope="module")
+def F():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_sparse_masked_02_gb300 import fdma
+
+    fdma.load()
+    return fdma
+
+
+def rel_l2(x, ref):
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.linalg.norm(ref)
+    return np.linalg.norm(x - ref) / (den if den > 0 else 1.0)
+
+
+def _cuda(t):
+    return None if t is None else t.cuda()
+
+
+def run_and_compare(F, inp, causal, scale, want_dbias=True, flags=0, check_bwd=True):
+    q, k, v, do = (_cuda(inp[n]) for n in ("q", "k", "v", "dout"))
+    bias, mask, cr = _cuda(inp.get("bias")), _cuda(inp.get("mask")), _cuda(inp.get("colranges"))
+    out, lse = F.fwd(q, k, v, mask=mask, colranges=cr, bias=bias, causal=causal, scale=scale, flags=flags)
+    if check_bwd:
+        dq, dk, dv, db = F.bwd(q, k, v, out, do, lse, mask=mask, colranges=cr, bias=bias, causal=causal, scale=scale,
+                               want_dbias=want_dbias, flags=flags)
+    assert F.device_error() == 0
+    p = orc.Problem(inp["q"], inp["k"], inp["v"], bias=inp.get("bias"), mask=inp.get("mask"),
+                    colranges=inp.get("colranges"), causal=causal, scale=scale, dout=inp["dout"])
+    O, L = orc.forward(p)
+    o_gpu = out.float().cpu().numpy()
+    l_gpu = lse.cpu().numpy()
+    empty = np.isneginf(L)
+    assert np.array_equal(np.isneginf(l_gpu), empty), "fully-masked rows disagree"
+    assert np.all(o_gpu.transpose(0, 2, 1, 3)[empty] == 0.0)
+    assert np.abs(o_gpu - O).max() <= O_MAXABS, np.abs(o_gpu - O).max()
+    assert rel_l2(o_gpu, O) <= O_RELL2, rel_l2(o_gpu, O)
+    fin = ~empty
+    assert np.abs(l_gpu[fin] - L[fin]).max(initial=0.0) <= LSE_ABS
+    if not check_bwd:
+        return
+    rq, rk, rv, rb = orc.backward(p, want_dbias=(db is not None))
+    for name, x, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        e = rel_l2(x.float().cpu().numpy(), ref)
+        assert e <= G_RELL2, (name, e)
+    if db is not None:
+        dbn = db.float().cpu().numpy()
+        e = rel_l2(dbn, rb)
+        assert e <= G_RELL2, ("dbias", e)
+        keep = np.zeros(rb.shape, dtype=bool)
+        for b in range(p.B):
+            for g in range(p.Hkv):
+                keep[b, g] = orc.keep_rows(p, b, g, 0, p.Nq)
+        assert np.all(dbn[~keep] == 0.0), "dbias must be exactly zero where keep is false"
+
+
+def test_quickstart_workload(F):
+    wl = W.WORKLOADS["tiny_n256_d64"]
+    run_and_compare(F, W.make_inputs(wl), True, wl.scale)
+
+
+def test_quickstart_workload_loss_sum(F):
+    wl = W.WORKLOADS["tiny_n256_d64"]
+    run_and_compare(F, W.make_inputs(wl, dout_ones=True), True, wl.scale)
+
+
+@pytest.mark.parametrize("N,Hq,Hkv,d,keep", [(512, 8, 2, 128, 256), (328, 4, 2, 128, 100), (384, 4, 4, 64, 64)])
+def test_causal_topk(F, N, Hq, Hkv, d, keep):
+    wl = W.scaled(W.WORKLOADS["n4096_hq32_hkv8"], Nq=N, Nk=N, Hq=Hq, Hkv=Hkv, d=d, keep_window=keep,
+                  scale=1 / math.sqrt(d), seed=77 + N)
+    run_and_compare(F, W.make_inputs(wl), True, wl.scale)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_noncausal_rect_random_mask(F, d):
+    g = torch.Generator().manual_seed(5 + d)
+    B, Nq, Nk, Hq, Hkv = 2, 200, 392, 4, 2
+    inp = dict(q=torch.randn(B, Nq, Hq, d, generator=g).bfloat16(), k=torch.randn(B, Nk, Hkv, d, generator=g).bfloat16(),
+               v=torch.randn(B, Nk, Hkv, d, generator=g).bfloat16(),
+               dout=torch.randn(B, Nq, Hq, d, generator=g).bfloat16(),
+               bias=torch.randn(B, Hkv, Nq, Nk, generator=g).bfloat16(),
+               mask=(torch.rand(B, Hkv, Nq, Nk, generator=g) < 0.3).bfloat16())
+    inp["mask"][0, 0, :, 128:256] = 0  # a fully skipped tile column
+    inp["mask"][1, 1, :128, :] = 1     # full tiles
+    inp["mask"][0, 1, 7, :] = 0        # one fully masked row
+    run_and_compare(F, inp, False, 0.1)
+
+
+def test_no_mask_no_bias(F):
+    g = torch.Generator().manual_seed(9)
+    B, N, Hq, Hkv, d = 1, 300, 2, 1, 64
+    inp = dict(q=torch.randn(B, N, Hq, d, generator=g).bfloat16(), k=torch.randn(B, N, Hkv, d, generator=g).bfloat16(),
+               v=torch.randn(B, N, Hkv, d, generator=g).bfloat16(),
+               dout=torch.randn(B, N, Hq, d, generator=g).bfloat16())
+    run_and_compare(F, inp, False, 0.125)
+    run_and_compare(F, inp, True, 0.125)
+
+
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_colranges_document_mask(F, with_bias):
+    wl = W.Workload("doc_small", 2, 1024, 1024, 4, 2, 128, True, 1 / math.sqrt(128), "colranges", 0, with_bias,
+                    doc_lo=64, doc_hi=300, seed=31)
+    inp = W.make_inputs(wl)
+    if with_bias:
+        inp["bias"] = torch.randn(2, 2, 1024, 1024, generator=torch.Generator().manual_seed(3)).bfloat16()
+    run_and_compare(F, inp, True, wl.scale)
+
+
+def test_colranges_random_ranges_noncausal(F):
+    g = torch.Generator().manual_seed(12)
+    B, N, Hq, Hkv, d = 1, 256, 2, 2, 128
+    s = torch.randint(-5, N, (B, Hkv, N), generator=g)
+    ln = torch.randint(-10, 200, (B, Hkv, N), generator=g)
+    cr = torch.stack([s, s + ln], -1).to(torch.int32).contiguous()
+    inp = dict(q=torch.randn(B, N, Hq, d, generator=g).bfloat16(), k=torch.randn(B, N, Hkv, d, generator=g).bfloat16(),
+               v=torch.randn(B, N, Hkv, d, generator=g).bfloat16(),
+               dout=torch.randn(B, N, Hq, d, generator=g).bfloat16(), colranges=cr)
+    run_and_compare(F, inp, False, 0.09)
+
+
+def test_bias_without_dbias(F):
+    wl = W.scaled(W.WORKLOADS["tiny_n256_d64"], seed=4)
+    run_and_compare(F, W.make_inputs(wl), True, wl.scale, want_dbias=False)
+
+
+def test_no_skip_flag_changes_nothing(F):
+    wl = W.scaled(W.WORKLOADS["n4096_hq32_hkv8"], Nq=512, Nk=512, Hq=4, Hkv=2, keep_window=64, seed=8)
+    inp = W.make_inputs(wl)
+    inp["mask"][0, 0, 256:, 0:128] = 0  # make some skippable tiles
+    run_and_compare(F, inp, True, wl.scale, flags=F.FDMA_FLAG_NO_SKIP)
+    q, k, v, do, bias, mask = (inp[n].cuda() for n in ("q", "k", "v", "dout", "bias", "mask"))
+    a = F.fwd(q, k, v, mask=mask, bias=bias, causal=True, scale=wl.scale)
+    b = F.fwd(q, k, v, mask=mask, bias=bias, causal=True, scale=wl.scale, flags=F.FDMA_FLAG_NO_SKIP)
+    assert (a[0].float() - b[0].float()).abs().max().item() <= 1e-2
+    ga = F.bwd(q, k, v, a[0], do, a[1], mask=mask, bias=bias, causal=True, scale=wl.scale)
+    gb = F.bwd(q, k, v, a[0], do, a[1], mask=mask, bias=bias, causal=True, scale=wl.scale,
+               flags=F.FDMA_FLAG_NO_SKIP)
+    for x, y in zip(ga, gb):
+        assert rel_l2(x.float().cpu().numpy(), y.float().cpu().numpy()) <= 1e-2
+
+
+@pytest.mark.parametrize("case", ["causal_topk", "ragged_rect", "colranges", "nomask_causal", "empty"])
+def test_block_map_bit_exact(F, case):
+    g = torch.Generator().manual_seed(21)
+    causal = case in ("causal_topk", "colranges", "nomask_causal")
+    Nq, Nk = (328, 328) if causal else (200, 520)
+    Hkv = 2
+    q = torch.randn(2, Nq, 4, 64, generator=g).bfloat16()
+    k = torch.randn(2, Nk, Hkv, 64, generator=g).bfloat16()
+    mask = cr = None
+    if case == "causal_topk":
+        bias = torch.randn(2, Hkv, Nq, Nk, generator=g).bfloat16()
+        mask = W.topk_mask_from_bias(bias, 40)
+        mask[1, 0, 128:256, 0:128] = 0
+    elif case == "ragged_rect":
+        mask = (torch.rand(2, Hkv, Nq, Nk, generator=g) < 0.002).bfloat16()
+        mask[0, 1] = 1
+    elif case == "colranges":
+        cr = W.doc_colranges(2, Hkv, Nk, 30, 150, 5)
+    elif case == "empty":
+        mask = torch.zeros(2, Hkv, Nq, Nk).bfloat16()
+    bm = F.classify_blocks(q.cuda(), k.cuda(), k.cuda(), mask=_cuda(mask), colranges=_cuda(cr), causal=causal)
+    p = orc.Problem(q, k, k, mask=mask, colranges=cr, causal=causal)
+    ref = orc.classify_blocks(p)
+    assert np.array_equal(bm.cpu().numpy(), ref)
+
+
+def test_reuse_classification(F):
+    wl = W.scaled(W.WORKLOADS["tiny_n256_d64"], seed=6)
+    inp = W.make_inputs(wl)
+    q, k, v, do, bias, mask = (inp[n].cuda() for n in ("q", "k", "v", "dout", "bias", "mask"))
+    args = F.make_args(q, k, v, mask=mask, bias=bias, causal=True, scale=wl.scale)
+    ws = F.alloc_workspace(args, True, q.device)
+    F.classify_blocks(q, k, v, mask=mask, causal=True, workspace=ws)
+    o1, l1 = F.fwd(q, k, v, mask=mask, bias=bias, causal=True, scale=wl.scale, workspace=ws,
+                   flags=F.FDMA_FLAG_REUSE_CLASSIFICATION)
+    o2, l2 = F.fwd(q, k, v, mask=mask, bias=bias, causal=True, scale=wl.scale)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    g1 = F.bwd(q, k, v, o1, do, l1, mask=mask, bias=bias, causal=True, scale=wl.scale, workspace=ws,
+               flags=F.FDMA_FLAG_REUSE_CLASSIFICATION)
+    g2 = F.bwd(q, k, v, o1, do, l1, mask=mask, bias=bias, causal=True, scale=wl.scale)
+    for x, y in zip(g1[1:], g2[1:]):
+        assert torch.equal(x, y)
+    assert rel_l2(g1[0].float().cpu().numpy(), g2[0].float().cpu().numpy()) < 1e-2
+
+
+def test_argument_errors(F):
+    q = torch.zeros(1, 128, 2, 64, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 128, 1, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(F.FdmaError) as e:
+        F.fwd(q, k, k, causal=False, scale=float("nan"))
+    assert e.value.status == F.FDMA_ERR_INVALID
+    q3 = torch.zeros(1, 128, 3, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(F.FdmaError) as e:
+        F.fwd(q3, torch.zeros(1, 128, 2, 64, dtype=torch.bfloat16, device="cuda"),
+              torch.zeros(1, 128, 2, 64, dtype=torch.bfloat16, device="cuda"))
+    assert e.value.status == F.FDMA_ERR_INVALID
+    q96 = torch.zeros(1, 128, 2, 96, dtype=torch.bfloat16, device="cuda")
+    k96 = torch.zeros(1, 128, 1, 96, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(F.FdmaError) as e:
+        F.fwd(q96, k96, k96)
+    assert e.value.status == F.FDMA_ERR_UNSUPPORTED
+    with pytest.raises(F.FdmaError) as e:
+        F.fwd(q, torch.zeros(1, 256, 1, 64, dtype=torch.bfloat16, device="cuda"),
+              torch.zeros(1, 256, 1, 64, dtype=torch.bfloat16, device="cuda"), causal=True)
+    assert e.value.status == F.FDMA_ERR_UNSUPPORTED

@@ -1,0 +1,93 @@
+"""Host-side checks of the C-ABI library that need no GPU: it builds, loads,
+exports every entry point include/fdma.h declares, and rejects bad arguments
+before touching the device."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+from block_sparse_masked_02_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fdma.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"FDMA_API\s+[\w\s\*]+?\b(fdma_\w+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def F():
+    if not os.path.exists(B.LIB) and shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("no nvcc to build libfdma")
+    B.build()
+    from block_sparse_masked_02_gb300 import fdma
+
+    return fdma
+
+
+def test_header_declares_the_entry_points():
+    assert _declared() == sorted(["fdma_workspace_size", "fdma_classify_blocks", "fdma_fwd", "fdma_bwd",
+                                  "fdma_get_device_error", "fdma_status_string"])
+
+
+def test_library_exports_every_declared_symbol(F):
+    lib = ctypes.CDLL(B.LIB)
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(F.EXPORTED) == set(_declared())
+
+
+def test_status_strings(F):
+    assert F.status_string(0) == "ok"
+    assert "workspace" in F.status_string(F.FDMA_ERR_WORKSPACE)
+    assert F.status_string(99) == "unknown status"
+
+
+def _args(F, **kw):
+    a = F.FdmaArgs()
+    a.B, a.Nq, a.Nk, a.Hq, a.Hkv, a.d = 1, 256, 256, 4, 2, 128
+    fake = 1 << 20  # never dereferenced: validation fails first or the size is pure arithmetic
+    a.q = a.k = a.v = fake
+    a.q_stride[:] = [256 * 4 * 128, 4 * 128, 128]
+    a.k_stride[:] = [256 * 2 * 128, 2 * 128, 128]
+    a.v_stride[:] = [256 * 2 * 128, 2 * 128, 128]
+    a.scale = 0.088
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_workspace_size_arithmetic(F):
+    a = _args(F)
+    lib = F.load()
+    fwd = lib.fdma_workspace_size(ctypes.byref(a), 0)
+    bwd = lib.fdma_workspace_size(ctypes.byref(a), 1)
+    tiles = 1 * 2 * 2 * 2
+    assert fwd >= tiles + 2 * tiles * 128 * 16
+    assert bwd >= fwd + 2 * (4 * 256 * 4) + 256 * 4 * 128 * 4
+    assert lib.fdma_workspace_size(ctypes.byref(_args(F, d=96)), 0) == 0
+    assert lib.fdma_workspace_size(ctypes.byref(_args(F, Hq=3)), 0) == 0
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("scale", float("nan"), 1), ("scale", -1.0, 1), ("Hq", 3, 1), ("d", 96, 2), ("Nk", 0, 1),
+    ("mask_kind", 7, 1), ("mask_kind", 1, 1), ("is_causal", 1, 2),
+])
+def test_argument_validation_before_any_cuda_call(F, field, value, status):
+    a = _args(F, **{field: value})
+    if field == "is_causal":
+        a.Nk = 384
+    lib = F.load()
+    rc = lib.fdma_fwd(ctypes.byref(a), 1 << 20, 1 << 20, None)
+    assert rc == status
+
+
+def test_missing_workspace_is_reported(F):
+    a = _args(F)
+    lib = F.load()
+    assert lib.fdma_fwd(ctypes.byref(a), 1 << 20, 1 << 20, None) == F.FDMA_ERR_WORKSPACE
+    assert lib.fdma_classify_blocks(ctypes.byref(a), 128, 128, None, None) == F.FDMA_ERR_WORKSPACE
