@@ -1,0 +1,426 @@
+"""Benchmark of the masked / biased attention hot path on GB300.
+
+One step = block classification + forward (O, lse) + backward (dQ, dK, dV,
+dBias) of one batch of the synthetic N=16384 workload (B=1, Hq=16, Hkv=4,
+d=128, causal, per-row top-2048 mask built from an N(0,1) bias).  The metric
+is effective fwd+bwd TFLOP/s counted over non-skipped 128x128 tiles:
+(4 + 10) * d * 128^2 * (active tiles) * (Hq / Hkv) per step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With N > 1 (torchrun, one process per GPU) every rank runs its own copy of
+the workload (weak scaling, no collective on the data path) and rank 0 prints
+the aggregate.  --impl reference times the fp64 CPU oracle on a bounded
+sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "n16384_hq16_hkv4"
+METRIC = "effective fwd+bwd TFLOP/s (non-skipped tiles) and % of roofline, 1 GB300"
+TILE = 128
+KERNELS_PER_STEP = 5  # classify, fwd, bwd_pre, bwd, dq_convert
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        exe = shutil.which("nvidia-smi")
+        if exe is None:
+            return self
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        self.fh = open(self.path, "w")
+        self.proc = subprocess.Popen([exe, "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                                      "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                                     stderr=subprocess.DEVNULL)
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def algorithmic_bytes(wl, bm):
+    """Minimum bytes the path must move (mask once over causally allowed tiles,
+    bias in fwd and bwd over active tiles, dBias over all of N^2, Q K V O dO dQ
+    dK dV and lse once each)."""
+    import numpy as np
+
+    tile_elems = TILE * TILE
+    nq_t, nk_t = bm.shape[2], bm.shape[3]
+    causal_tiles = sum(1 for qt in range(nq_t) for kt in range(nk_t) if kt <= qt) * wl.B * wl.Hkv
+    active = int((bm != 0).sum())
+    mask_b = causal_tiles * tile_elems * 2
+    bias_b = 2 * active * tile_elems * 2
+    dbias_b = wl.B * wl.Hkv * wl.Nq * wl.Nk * 2
+    io = 2 * (4 * wl.B * wl.Nq * wl.Hq * wl.d + 4 * wl.B * wl.Nk * wl.Hkv * wl.d) + 4 * wl.B * wl.Hq * wl.Nq
+    return {"mask": mask_b, "bias": bias_b, "dbias": dbias_b, "io": io, "total": mask_b + bias_b + dbias_b + io,
+            "bwd_kernel": active * tile_elems * 2 + dbias_b + 2 * (3 * wl.B * wl.Nq * wl.Hq * wl.d +
+                                                                    2 * wl.B * wl.Nk * wl.Hkv * wl.d)}
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    from block_sparse_masked_02_gb300 import fdma, workloads as W
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    fdma.load()
+    wl = W.WORKLOADS[WORKLOAD]
+    dev = torch.device("cuda", local)
+    inp = W.make_inputs(wl, device=dev, seed=wl.seed + rank)
+    q, k, v, do, bias, mask = (inp[n] for n in ("q", "k", "v", "dout", "bias", "mask"))
+    a = fdma.make_args(q, k, v, mask=mask, bias=bias, causal=True, scale=wl.scale)
+    wsp = fdma.alloc_workspace(a, True, dev)
+    bm = fdma.classify_blocks(q, k, v, mask=mask, causal=True, workspace=wsp)
+    active = int((bm != 0).sum().item())
+    partial = int((bm == 1).sum().item())
+    full = int((bm == 2).sum().item())
+    flops_fwd = 4.0 * wl.d * TILE * TILE * active * wl.G
+    flops_bwd = 10.0 * wl.d * TILE * TILE * active * wl.G
+    flops = flops_fwd + flops_bwd
+    out = torch.empty_like(q)
+    lse = torch.empty((wl.B, wl.Hq, wl.Nq), dtype=torch.float32, device=dev)
+    grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(bias))
+    stream = torch.cuda.current_stream()
+    R = fdma.FDMA_FLAG_REUSE_CLASSIFICATION
+
+    def step():
+        fdma.classify_blocks(q, k, v, mask=mask, causal=True, workspace=wsp)
+        fdma.fwd(q, k, v, mask=mask, bias=bias, causal=True, scale=wl.scale, workspace=wsp, flags=R, out=out,
+                 lse=lse)
+        fdma.bwd(q, k, v, out, do, lse, mask=mask, bias=bias, causal=True, scale=wl.scale, workspace=wsp, flags=R,
+                 grads=grads)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fdma.device_error() != 0:
+        raise RuntimeError("kernel-side error during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local] if ws > 1 else \
+        os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            e = ev[i]
+            e[0].record(stream)
+            fdma.classify_blocks(q, k, v, mask=mask, causal=True, workspace=wsp)
+            e[1].record(stream)
+            fdma.fwd(q, k, v, mask=mask, bias=bias, causal=True, scale=wl.scale, workspace=wsp, flags=R, out=out,
+                     lse=lse)
+            e[2].record(stream)
+            fdma.bwd(q, k, v, out, do, lse, mask=mask, bias=bias, causal=True, scale=wl.scale, workspace=wsp,
+                     flags=R, grads=grads)
+            e[3].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    ms_total = t0.elapsed_time(t1)
+    ms_cls = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    ms_fwd = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    ms_bwd = sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps
+    err = fdma.device_error()
+
+    # ---- end to end: pinned host inputs in, results out, through the same C-ABI calls
+    host_in = {n: inp[n].cpu().pin_memory() for n in ("q", "k", "v", "dout", "mask", "bias")}
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (out, lse, *grads)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e2e_steps = max(1, min(args.steps, 5))
+    dev_in = {n: torch.empty_like(inp[n]) for n in host_in}
+
+    def e2e_step():
+        for n, t in host_in.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        fdma.classify_blocks(dev_in["q"], dev_in["k"], dev_in["v"], mask=dev_in["mask"], causal=True, workspace=wsp)
+        fdma.fwd(dev_in["q"], dev_in["k"], dev_in["v"], mask=dev_in["mask"], bias=dev_in["bias"], causal=True,
+                 scale=wl.scale, workspace=wsp, flags=R, out=out, lse=lse)
+        fdma.bwd(dev_in["q"], dev_in["k"], dev_in["v"], out, dev_in["dout"], lse, mask=dev_in["mask"],
+                 bias=dev_in["bias"], causal=True, scale=wl.scale, workspace=wsp, flags=R, grads=grads)
+        for h, d in zip(host_out, (out, lse, *grads)):
+            h.copy_(d, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = s0.elapsed_time(s1) / e2e_steps
+
+    times = torch.tensor([ms_total, ms_e2e, ms_bwd, ms_fwd, ms_cls], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    ms_total, ms_e2e, ms_bwd, ms_fwd, ms_cls = times.tolist()
+    if rank != 0:
+        dist.destroy_process_group()
+        return None
+
+    peaks = _peaks()
+    ms_step = ms_total / args.steps
+    value = flops * ws / (ms_step * 1e-3) / 1e12
+    bw = algorithmic_bytes(wl, bm.cpu().numpy())
+    roof_ms = max(flops / (peaks["bf16_tflops_sustained"] * 1e12), bw["total"] / (peaks["hbm_gbs"] * 1e9)) * 1e3
+    bwd_achieved = flops_bwd / (ms_bwd * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": wl.B, "N": wl.Nq, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+                   "mask": f"causal and per-row top-{wl.keep_window} of an N(0,1) bias", "dbias": True,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (mask + bias 4.3 GB per step)",
+                   "tiles": {"active": active, "partial": partial, "full": full, "total": int(bm.numel()),
+                             "skip_ratio": round(1 - active / bm.numel(), 4)}},
+        "pct_of_roofline": round(100.0 * roof_ms / ms_step, 2),
+        "breakdown_ms": {"classify": round(ms_cls, 4), "fwd": round(ms_fwd, 4), "bwd": round(ms_bwd, 4)},
+        "roofline": {"kernel": "bwd (fdma_bwd: bwd_pre + bwd_kernel + dq_convert)", "bound": "tensor",
+                     "achieved": round(bwd_achieved, 2),
+                     "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "peak_source": peaks["source"] + " bf16_tflops_sustained",
+                     "frac": round(bwd_achieved / peaks["bf16_tflops_sustained"], 4),
+                     "traffic": None},
+        "e2e": {"value": round(flops * ws / (ms_e2e * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3)},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clk.summary(),
+        "device_error": err,
+    }
+    if not args.no_cpu_baseline:
+        host, bw_, mw_ = _gpu_windows(inp, wl)
+        line["cpu_baseline"] = cpu_baseline(host, bw_, mw_, wl, seconds=args.cpu_seconds)
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
+class _RowWindow:
+    """Host copy of rows [r0, r0 + R) of (batch 0, kv head 0) of a (B,Hkv,Nq,Nk)
+    tensor; the oracle only indexes inside that window."""
+
+    def __init__(self, rows, r0, shape):
+        self.shape = tuple(shape)
+        self.r0 = r0
+        self.data = rows
+
+    def __getitem__(self, idx):
+        b, g, rs, cs = idx
+        assert b == 0 and g == 0 and rs.start >= self.r0
+        return self.data[rs.start - self.r0:rs.stop - self.r0, cs]
+
+
+def cpu_baseline(host, bias_win, mask_win, wl, seconds=15.0, max_tiles=None):
+    """Times the fp64 oracle (as written, no tuning) on whole 128-row query
+    tiles of kv group 0 (all its query heads), last (longest causal) tiles
+    first, until about `seconds` of CPU time or `max_tiles`; the rate counts
+    the sample's non-skipped tiles exactly like the GPU metric."""
+    from oracle import attention as orc
+
+    nqt = -(-wl.Nq // TILE)
+    nkt = -(-wl.Nk // TILE)
+    done = active = 0
+    t_used = 0.0
+    qt = nqt - 1
+    while qt >= 0 and qt * TILE >= bias_win.r0 and (t_used < seconds or done == 0):
+        if max_tiles is not None and done >= max_tiles:
+            break
+        r0, r1 = qt * TILE, min((qt + 1) * TILE, wl.Nq)
+        p = orc.Problem(host["q"], host["k"], host["v"], bias=bias_win, mask=mask_win, causal=True, scale=wl.scale,
+                        dout=host["dout"])
+        t0 = time.perf_counter()
+        kv = orc._kv(p, 0, 0)
+        keep = orc.keep_rows(p, 0, 0, r0, r1)
+        for h in range(wl.G):
+            orc.forward_rows(p, 0, h, r0, r1, kv, keep)
+        orc.backward_rows(p, 0, 0, r0, r1, kv, keep)
+        t_used += time.perf_counter() - t0
+        active += sum(int(keep[:, kt * TILE:(kt + 1) * TILE].any()) for kt in range(nkt))
+        done += 1
+        qt -= 1
+    flops = 14.0 * wl.d * TILE * TILE * active * wl.G
+    return {"value": round(flops / t_used / 1e12, 6), "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"{done} query tile(s) x {wl.G} heads of kv group 0 ({active} active tiles), fwd+bwd, "
+                      f"{t_used:.2f} s; numpy float64 (BLAS threads = host cores)",
+            "seconds": round(t_used, 3)}
+
+
+def _gpu_windows(inp, wl, tiles=16):
+    r0 = max(0, wl.Nq - tiles * TILE)
+    host = {n: inp[n].cpu() for n in ("q", "k", "v", "dout")}
+    bw = _RowWindow(inp["bias"][0, 0, r0:].cpu(), r0, inp["bias"].shape)
+    mw = _RowWindow(inp["mask"][0, 0, r0:].cpu(), r0, inp["mask"].shape)
+    return host, bw, mw
+
+
+def _host_windows(wl, tiles):
+    """The workload's recipe drawn on the host for the sampled rows only: full
+    Q, K, V, dO and the last `tiles` query tiles of kv group 0's bias / mask."""
+    import torch
+
+    from block_sparse_masked_02_gb300 import workloads as W
+
+    g = torch.Generator().manual_seed(wl.seed)
+    host = {
+        "q": torch.randn((wl.B, wl.Nq, wl.Hq, wl.d), generator=g).to(torch.bfloat16),
+        "k": torch.randn((wl.B, wl.Nk, wl.Hkv, wl.d), generator=g).to(torch.bfloat16),
+        "v": torch.randn((wl.B, wl.Nk, wl.Hkv, wl.d), generator=g).to(torch.bfloat16),
+        "dout": torch.randn((wl.B, wl.Nq, wl.Hq, wl.d), generator=g).to(torch.bfloat16),
+    }
+    r0 = max(0, wl.Nq - tiles * TILE)
+    bias = torch.randn((1, 1, wl.Nq - r0, wl.Nk), generator=g).to(torch.bfloat16)
+    mask = W.topk_mask_from_bias(bias, wl.keep_window)
+    bias.masked_fill_(mask == 0, W.BF16_MIN)
+    shape = (wl.B, wl.Hkv, wl.Nq, wl.Nk)
+    return host, _RowWindow(bias[0, 0], r0, shape), _RowWindow(mask[0, 0], r0, shape)
+
+
+def run_reference(args):
+    """--impl reference: the fp64 CPU oracle, as written, is the reference arm."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return None
+    from block_sparse_masked_02_gb300 import workloads as W
+
+    wl = W.WORKLOADS[WORKLOAD]
+    host, bw, mw = _host_windows(wl, tiles=1)
+    for _ in range(args.warmup):
+        cpu_baseline(host, bw, mw, wl, seconds=0.0, max_tiles=1)
+    rates, secs = [], []
+    for _ in range(args.steps):
+        r = cpu_baseline(host, bw, mw, wl, seconds=0.0, max_tiles=1)
+        rates.append(r["value"])
+        secs.append(r["seconds"])
+    value = statistics.median(rates)
+    ms_step = 1e3 * statistics.median(secs)
+    return {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 1), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": WORKLOAD, "B": wl.B, "N": wl.Nq, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+                   "mask": f"causal and per-row top-{wl.keep_window} of an N(0,1) bias", "dbias": True},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                         "sample": f"each step: the last query tile x {wl.G} heads of kv group 0 (fwd+bwd), "
+                                   "rows drawn on the host with the workload's recipe"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

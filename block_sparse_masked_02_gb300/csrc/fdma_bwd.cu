@@ -13,14 +13,16 @@
 //                      dP^T = V dO^T          (SS, TMEM cols 128..255)
 //                      P^T  = exp2(S^T*c + bias^T*log2e - lse2)   (mask bits)
 //                      dS^T = P^T (dP^T - delta)
-//                      dV  += P^T dO          (TS: P^T from TMEM)
+//                      dV  += P^T dO          (TS: P^T packed in TMEM cols 0..31, 64..95)
 //                      dK  += dS^T Q          (SS: dS^T staged in smem)
 //                      dQ   = dS K            (SS, reuses TMEM cols 128..)
 //                    dQ is added to an fp32 accumulator with vector
 //                    reductions; dBias = sum over the group's heads of dS is
-//                    kept in registers (one thread per key) and written once
-//                    per (query tile, key tile); skipped tiles of dBias are
-//                    written as zeros by the same CTA.
+//                    kept in registers (one thread per key and half of the
+//                    query tile) and written once per (query tile, key tile);
+//                    the bias^T slice is loaded once per query tile for all
+//                    heads; skipped tiles of dBias are written as zeros by the
+//                    same CTA.  Warps: 0 TMA, 1 MMA, 4..11 two compute groups.
 //   dq_convert       fp32 accumulator -> bf16 dQ.
 #include "fdma_internal.h"
 #include "fdma_ptx.cuh"
@@ -105,6 +107,11 @@ enum BwdBar : int {
   kNumBwdBars = 13
 };
 
+// 12 warps: warpgroup 0 = {TMA producer, MMA issuer, 2 idle}, warpgroups 1-2 = compute.
+constexpr int kBwdThreads = 384;
+constexpr uint32_t kRegsLow = 104, kRegsHigh = 200;
+constexpr int kBwdMinLaunchRegs = (kRegsLow + 2 * kRegsHigh) / 3;  // 168
+
 template <int D>
 struct BwdSmem {
   static constexpr uint32_t kQB = 128u * D * 2u;
@@ -138,7 +145,7 @@ struct ColIter {
 };
 
 template <int D, bool HAS_BIAS, bool WANT_DBIAS>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                const BwdParams p) {
@@ -179,8 +186,8 @@ __global__ void __launch_bounds__(192, 1)
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBwdBars; ++i) mbar_init(&bars[i], 1);
-    mbar_init(&bars[kPReady], 128);
-    mbar_init(&bars[kDqFree], 128);
+    mbar_init(&bars[kPReady], 256);
+    mbar_init(&bars[kDqFree], 256);
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -195,7 +202,9 @@ __global__ void __launch_bounds__(192, 1)
   const int first_qt = it.next(-1);
   const bool any_active = first_qt < p.nTq;
 
-  if (warp == 0) {
+  if (warp < 4) {
+   regs_decrease<kRegsLow>();
+   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && any_active) {
       tma_prefetch_desc(&tmQ);
@@ -272,7 +281,8 @@ __global__ void __launch_bounds__(192, 1)
           // dV += P^T dO ; dK += dS^T Q   (K dimension = 128 queries)
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            umma_ts(tbase + 256, tbase + k * 8, dodesc_mn + mnmajor_step(k), IDESC_DV, (n > 0 || k > 0) ? 1u : 0u);
+            umma_ts(tbase + 256, tbase + k * 8 + (k >= 4 ? 32 : 0), dodesc_mn + mnmajor_step(k), IDESC_DV,
+                    (n > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             umma_ss(tbase + 384, dsdesc_k + kmajor_step(k, 128), qdesc_mn + mnmajor_step(k), IDESC_DK,
@@ -290,29 +300,54 @@ __global__ void __launch_bounds__(192, 1)
       umma_commit(&bars[kDrain]);
       mbar_wait(&bars[kDrain], 0, p.err, kDevErrTimeout, nullptr);
     }
+   }
   } else {
+   regs_increase<kRegsHigh>();
+   {
     // ------------------------------------------------------------ compute
+    // Two warpgroups: wg 0 owns queries 0..63 of every step, wg 1 queries 64..127.
+    // Thread (quad, lane) owns key row j of S^T/dP^T/dK/dV and query row j of dQ.
+    const int wg = (warp - 4) >> 2;
     const int quad = warp & 3;
-    const int j = quad * 32 + lane;  // key row of S^T / dP^T / dK / dV; query row of dQ
+    const int j = quad * 32 + lane;
+    const int ctid = (warp - 4) * 32 + lane;  // 0..255
     const int kidx = k0 + j;
     const bool kin = kidx < p.Nk;
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
-    float acc[WANT_DBIAS ? 128 : 1];
+    const int qbase = wg * 64;
+    float acc[WANT_DBIAS ? 64 : 1];
 #pragma unroll
-    for (int c = 0; c < (WANT_DBIAS ? 128 : 1); ++c) acc[c] = 0.f;
+    for (int c = 0; c < (WANT_DBIAS ? 64 : 1); ++c) acc[c] = 0.f;
     int n = 0;
     bool ok = true;
     for (int qt = first_qt; ok && qt < p.nTq; qt = it.next(qt)) {
       const int q0 = qt * kTile;
       const int64_t tile = col_base + static_cast<int64_t>(qt) * p.nTk;
-      const bool partial =
-          p.kmap[tile] == kPartial || ragged_k || (ragged_q_any && qt == p.nTq - 1);
-      uint4 bits = make_uint4(~0u, ~0u, ~0u, ~0u);
-      if (partial) bits = __ldg(&p.bits_col[tile * kTile + j]);
-      const uint32_t bw[4] = {bits.x, bits.y, bits.z, bits.w};
-      const uint16_t* bcol = nullptr;
-      if (HAS_BIAS) bcol = p.bias + b * p.bs_b + g * p.bs_h + static_cast<int64_t>(q0) * p.bs_r + kidx;
-      const int rows_in = min(kTile, p.Nq - q0);
+      const bool partial = p.kmap[tile] == kPartial || ragged_k || (ragged_q_any && qt == p.nTq - 1);
+      uint32_t bw0 = ~0u, bw1 = ~0u;  // keep bits of queries qbase..qbase+63 for key j
+      if (partial) {
+        const uint2 bb = reinterpret_cast<const uint2*>(&p.bits_col[tile * kTile + j])[wg];
+        bw0 = bb.x;
+        bw1 = bb.y;
+      }
+      const int rows_in = min(kTile, p.Nq - q0) - qbase;  // valid queries in this half
+      // bias^T column slice, loaded once per query tile and reused by every head of the group
+      uint32_t bpk[HAS_BIAS ? 32 : 1];
+      if (HAS_BIAS) {
+        const uint16_t* bcol = p.bias + b * p.bs_b + g * p.bs_h + static_cast<int64_t>(q0 + qbase) * p.bs_r + kidx;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint16_t braw[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int qi = half * 32 + e;
+            braw[e] = (kin && qi < rows_in) ? __ldg(bcol + static_cast<int64_t>(qi) * p.bs_r) : static_cast<uint16_t>(0);
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            bpk[half * 16 + e] = static_cast<uint32_t>(braw[2 * e]) | (static_cast<uint32_t>(braw[2 * e + 1]) << 16);
+        }
+      }
       for (int hh = 0; hh < p.G; ++hh, ++n) {
         const int h = g * p.G + hh;
         const int s = n & 1;
@@ -321,20 +356,14 @@ __global__ void __launch_bounds__(192, 1)
         if (!(ok = mbar_wait(&bars[kQdoFull + s], (n >> 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
         if (n > 0 && !(ok = mbar_wait(&bars[kDsFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
         tc_fence_after();
-        const float* lse2 = sLse + s * 128;
-        const float* dlt = sDelta + s * 128;
+        const float* lse2 = sLse + s * 128 + qbase;
+        const float* dlt = sDelta + s * 128 + qbase;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {  // 16 queries per chunk
+        for (int c = 0; c < 4; ++c) {  // 16 queries per chunk
+          const int col = qbase + c * 16;
           uint32_t sr[16], dr[16];
-          tmem_ld16(tl + c * 16, sr);
-          tmem_ld16(tl + 128 + c * 16, dr);
-          float bv[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            bv[e] = 0.f;
-            if (HAS_BIAS && kin && (c * 16 + e) < rows_in)
-              bv[e] = bf16_to_f32(__ldg(bcol + static_cast<int64_t>(c * 16 + e) * p.bs_r));
-          }
+          tmem_ld16(tl + col, sr);
+          tmem_ld16(tl + 128 + col, dr);
           tmem_ld_wait();
           uint32_t pk[8], dk[8];
 #pragma unroll
@@ -342,9 +371,15 @@ __global__ void __launch_bounds__(192, 1)
             float pv[2], dv[2];
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-              const int qi = c * 16 + e + t;
-              const bool keep = (bw[qi >> 5] >> (qi & 31)) & 1u;
-              const float x = fmaf(__uint_as_float(sr[e + t]), p.scale_log2, fmaf(bv[e + t], kLog2e, -lse2[qi]));
+              const int qi = c * 16 + e + t;  // 0..63 within this half
+              const uint32_t word = qi < 32 ? bw0 : bw1;
+              const bool keep = (word >> (qi & 31)) & 1u;
+              float bval = 0.f;
+              if (HAS_BIAS) {
+                const uint32_t w2 = bpk[qi >> 1];
+                bval = __uint_as_float((qi & 1) ? (w2 & 0xFFFF0000u) : (w2 << 16));
+              }
+              const float x = fmaf(__uint_as_float(sr[e + t]), p.scale_log2, fmaf(bval, kLog2e, -lse2[qi]));
               pv[t] = keep ? ex2(x) : 0.f;
               dv[t] = pv[t] * (__uint_as_float(dr[e + t]) - dlt[qi]);
               if (WANT_DBIAS) acc[qi] += dv[t];
@@ -352,25 +387,27 @@ __global__ void __launch_bounds__(192, 1)
             pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
             dk[e >> 1] = pack_bf16x2(dv[0], dv[1]);
           }
-          tmem_st8(tl + c * 8, pk);
-          // dS^T row j, queries c*16..c*16+15: two 16-byte chunks of the SW128 K-major tile
-          uint8_t* rowp = sDS + (c >> 2) * 16384 + j * 128;
-          const int ch0 = (c & 3) * 2;
-          *reinterpret_cast<uint4*>(rowp + (((ch0) ^ (j & 7)) << 4)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
+          // packed P^T stays inside this warpgroup's own S^T columns (already read), so
+          // queries 0..63 -> cols 0..31 and queries 64..127 -> cols 64..95
+          tmem_st8(tl + wg * 64 + c * 8, pk);
+          // dS^T row j, queries col..col+15: two 16-byte chunks of the SW128 K-major tile
+          uint8_t* rowp = sDS + wg * 16384 + j * 128;
+          const int ch0 = c * 2;
+          *reinterpret_cast<uint4*>(rowp + ((ch0 ^ (j & 7)) << 4)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
           *reinterpret_cast<uint4*>(rowp + (((ch0 + 1) ^ (j & 7)) << 4)) = make_uint4(dk[4], dk[5], dk[6], dk[7]);
         }
         fence_proxy_async_smem();
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars[kPReady]);
-        // drain dQ: this thread owns query row q0 + j
+        // drain dQ: query row q0 + j, this warpgroup's half of the head dim
         if (!(ok = mbar_wait(&bars[kDqFull], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
         tc_fence_after();
-        float* dqrow = p.dq_acc + ((static_cast<int64_t>(b) * p.nqpad + q0 + j) * p.Hq + h) * D;
+        float* dqrow = p.dq_acc + ((static_cast<int64_t>(b) * p.nqpad + q0 + j) * p.Hq + h) * D + wg * (D / 2);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t r[32];
-          tmem_ld32(tl + 128 + c * 32, r);
+          tmem_ld32(tl + 128 + wg * (D / 2) + c * 32, r);
           tmem_ld_wait();
 #pragma unroll
           for (int v = 0; v < 8; ++v)
@@ -383,10 +420,11 @@ __global__ void __launch_bounds__(192, 1)
       }
       if (WANT_DBIAS && ok) {
         uint16_t* dcol = p.dbias + (static_cast<int64_t>(b) * p.Hkv + g) * p.Nq * p.Nk +
-                         static_cast<int64_t>(q0) * p.Nk + kidx;
+                         static_cast<int64_t>(q0 + qbase) * p.Nk + kidx;
 #pragma unroll
-        for (int qi = 0; qi < 128; ++qi) {
-          if (kin && qi < rows_in) dcol[static_cast<int64_t>(qi) * p.Nk] = static_cast<uint16_t>(pack_bf16x2(acc[qi], 0.f) & 0xFFFFu);
+        for (int qi = 0; qi < 64; ++qi) {
+          if (kin && qi < rows_in)
+            dcol[static_cast<int64_t>(qi) * p.Nk] = static_cast<uint16_t>(pack_bf16x2(acc[qi], 0.f) & 0xFFFFu);
           acc[qi] = 0.f;
         }
       }
@@ -394,46 +432,46 @@ __global__ void __launch_bounds__(192, 1)
     // zero-fill dBias tiles of this key column that were skipped
     if (WANT_DBIAS && ok) {
       const int cols = min(kTile, p.Nk - k0);
+      const int r = ctid & 127, half = ctid >> 7;
       for (int qt = 0; qt < p.nTq; ++qt) {
         if (p.kmap[col_base + static_cast<int64_t>(qt) * p.nTk] != kSkip) continue;
-        const int i = qt * kTile + j;
+        const int i = qt * kTile + r;
         if (i >= p.Nq) continue;
         uint16_t* drow = p.dbias + ((static_cast<int64_t>(b) * p.Hkv + g) * p.Nq + i) * p.Nk + k0;
-        for (int c = 0; c < cols; c += 8) *reinterpret_cast<uint4*>(drow + c) = make_uint4(0, 0, 0, 0);
+        for (int c = half * 64; c < min(cols, half * 64 + 64); c += 8)
+          *reinterpret_cast<uint4*>(drow + c) = make_uint4(0, 0, 0, 0);
       }
     }
-    // dK, dV
+    // dK (warpgroup 0) and dV (warpgroup 1)
     if (ok && n > 0) ok = mbar_wait(&bars[kFinal], 0, p.err, kDevErrTimeout, abort_flag);
     if (ok) {
       tc_fence_after();
       const int64_t off = ((static_cast<int64_t>(b) * p.Nk + kidx) * p.Hkv + g) * D;
+      uint16_t* dst = (wg == 0 ? p.dk : p.dv) + off;
+      const uint32_t col0 = wg == 0 ? 384u : 256u;
+      const float sc = wg == 0 ? p.scale : 1.f;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        uint16_t* dst = (which == 0 ? p.dk : p.dv) + off;
-        const uint32_t col0 = which == 0 ? 384u : 256u;
-        const float sc = which == 0 ? p.scale : 1.f;
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        if (n > 0) {
+          tmem_ld32(tl + col0 + c * 32, r);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          if (n > 0) {
-            tmem_ld32(tl + col0 + c * 32, r);
-            tmem_ld_wait();
-          } else {
+          for (int t = 0; t < 32; ++t) r[t] = 0u;
+        }
+        uint32_t pk[16];
 #pragma unroll
-            for (int t = 0; t < 32; ++t) r[t] = 0u;
-          }
-          uint32_t pk[16];
+        for (int t = 0; t < 16; ++t)
+          pk[t] = pack_bf16x2(__uint_as_float(r[2 * t]) * sc, __uint_as_float(r[2 * t + 1]) * sc);
+        if (kin) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-          for (int t = 0; t < 16; ++t)
-            pk[t] = pack_bf16x2(__uint_as_float(r[2 * t]) * sc, __uint_as_float(r[2 * t + 1]) * sc);
-          if (kin) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-          }
+          for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
     }
+  }
   }
   tc_fence_before();
   __syncthreads();
@@ -451,8 +489,13 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   auto kern = bwd_kernel<D, HB, WD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
   if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  // setmaxnreg re-balancing needs the launch allocation to cover 56 + 2 x 224 per SMSP slot
+  if (fa.numRegs < kBwdMinLaunchRegs) return cudaErrorInvalidConfiguration;
   const unsigned grid = static_cast<unsigned>(p.nTk) * p.B * p.Hkv;
-  kern<<<grid, 192, L::kTotal, stream>>>(tq, tk, tv, tdo, p);
+  kern<<<grid, kBwdThreads, L::kTotal, stream>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }
 

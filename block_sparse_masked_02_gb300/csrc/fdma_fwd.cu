@@ -283,9 +283,13 @@ __global__ void __launch_bounds__(192, 1)
         for (int c = 0; c < 128; ++c)
           if (!((bw[c >> 5] >> (c & 31)) & 1u)) x[c] = kNegInf;
       }
-      float mx = x[0];
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+      for (int t = 0; t < 8; ++t) mx8[t] = x[t];
+#pragma unroll
+      for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m_ref, mx);
       float alpha = 1.f;
       bool resc = false;
@@ -319,7 +323,7 @@ __global__ void __launch_bounds__(192, 1)
         tmem_st_wait();
       }
       const float mu = (m_ref == kNegInf) ? 0.f : m_ref;
-      float sum = 0.f;
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
@@ -327,12 +331,13 @@ __global__ void __launch_bounds__(192, 1)
         for (int j = 0; j < 16; ++j) {
           const float p0 = ex2(x[c * 32 + 2 * j] - mu);
           const float p1 = ex2(x[c * 32 + 2 * j + 1] - mu);
-          sum += p0 + p1;
           pk[j] = pack_bf16x2(p0, p1);
+          // normalise with the same bf16-rounded weights the PV product uses
+          sum4[j & 3] += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xFFFF0000u);
         }
         tmem_st16(tl + s * 128 + c * 16, pk);
       }
-      l += sum;
+      l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars[kPReady + s]);

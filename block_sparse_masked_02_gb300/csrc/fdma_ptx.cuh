@@ -254,6 +254,20 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
+// ---------------------------------------------------------------- register re-balancing
+// setmaxnreg moves registers between the warpgroups of a CTA.  The sum over
+// warpgroups must not exceed what the CTA was launched with (threads x
+// registers per thread), or the increasing warpgroup waits forever; the host
+// launchers check the compiled register count before every launch.
+template <uint32_t N>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------------------------- packing
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;

@@ -160,7 +160,9 @@ def workspace_size(args: FdmaArgs, for_bwd: bool) -> int:
 def alloc_workspace(args: FdmaArgs, for_bwd: bool, device) -> torch.Tensor:
     n = workspace_size(args, for_bwd)
     if n == 0:
-        raise FdmaError(FDMA_ERR_INVALID, "fdma_workspace_size")
+        # invalid shape: let the entry point name the problem (no workspace attached)
+        st = load().fdma_fwd(ctypes.byref(args), None, None, None)
+        raise FdmaError(st if st != FDMA_OK else FDMA_ERR_INVALID, "fdma_workspace_size")
     ws = torch.empty(n + 256, dtype=torch.uint8, device=device)
     off = (-ws.data_ptr()) % 256
     return ws[off:off + n]

@@ -2,9 +2,11 @@
 the fp64 oracle on seeded inputs that span several tiles and ragged tails.
 
 Tolerances: block map bit-exact; O max-abs <= 1e-2 and rel-L2 <= 5e-3;
-dQ, dK, dV, dBias rel-L2 <= 1e-2 (bf16 inputs, fp32 accumulation); lse is
-compared to 2e-3 absolute, and rows with no kept key must give lse = -inf and
-O = 0 exactly."""
+dQ, dK, dV, dBias rel-L2 <= 1e-2 (bf16 inputs, fp32 accumulation).  The
+kernel normalises O with the sum of the same bf16-rounded weights that enter
+the P V product, so its log-sum-exp differs from the exact one by at most
+ln(1 + 2^-9) ~ 1.95e-3 plus fp32 rounding: lse is compared to 4e-3 absolute.
+Rows with no kept key must give lse = -inf and O = 0 exactly."""
 import math
 
 import numpy as np
@@ -16,7 +18,7 @@ from block_sparse_masked_02_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-O_MAXABS, O_RELL2, G_RELL2, LSE_ABS = 1e-2, 5e-3, 1e-2, 2e-3
+O_MAXABS, O_RELL2, G_RELL2, LSE_ABS = 1e-2, 5e-3, 1e-2, 4e-3
 
 
 @pytest.fixture(scope="module")
