@@ -32,7 +32,7 @@ FDMA_FLAG_NO_SKIP = 2
 TILE = 128
 
 EXPORTED = ("fdma_workspace_size", "fdma_classify_blocks", "fdma_fwd", "fdma_bwd", "fdma_get_device_error",
-            "fdma_status_string")
+            "fdma_status_string", "fdma_fwd_noalloc")
 
 
 class FdmaArgs(ctypes.Structure):
@@ -88,6 +88,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.fdma_get_device_error.restype = ctypes.c_int
     lib.fdma_status_string.argtypes = [ctypes.c_int]
     lib.fdma_status_string.restype = ctypes.c_char_p
+    lib.fdma_fwd_noalloc.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    lib.fdma_fwd_noalloc.restype = ctypes.c_int
     _LIB = lib
     return lib
 
@@ -233,3 +235,20 @@ def bwd(q, k, v, out, dout, lse, *, mask=None, colranges=None, bias=None, causal
 def device_error(stream=None) -> int:
     """Synchronize and return (then clear) the first kernel-side error status."""
     return int(load().fdma_get_device_error(_stream_ptr(stream)))
+
+
+def fwd_noalloc(q, k, v, *, mask=None, colranges=None, bias=None, causal=False, scale=None, flags=0, out=None,
+                lse=None, stream=None):
+    """Forward through fdma_fwd_noalloc: the library's fixed 16 MiB device array serves as
+    the workspace, so nothing is allocated for it (out and lse are allocated here only when
+    not given).  Returns (out, lse)."""
+    _check_cuda(q, k, v, mask, colranges, bias)
+    args = make_args(q, k, v, mask=mask, colranges=colranges, bias=bias, causal=causal, scale=scale, flags=flags)
+    B, Nq, Hq, d = q.shape
+    if out is None:
+        out = torch.empty((B, Nq, Hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    _raise(load().fdma_fwd_noalloc(ctypes.byref(args), out.data_ptr(), lse.data_ptr(), _stream_ptr(stream)),
+           "fdma_fwd_noalloc")
+    return out, lse

@@ -136,6 +136,24 @@ FDMA_API int fdma_fwd(const fdma_args* args, void* out, float* lse, void* stream
 FDMA_API int fdma_bwd(const fdma_args* args, const void* out, const void* dout, const float* lse, void* dq, void* dk,
              void* dv, void* dbias, void* stream);
 
+/* Forward without a caller-provided workspace, for callers that cannot allocate device
+   memory when they call it (an allocator or memory-pool callback, a plugin handed only
+   fixed buffers, a process whose device footprint must not grow after start-up).  The
+   pages describe no such entry point; it has no counterpart there.
+   Same operation, arguments and outputs as fdma_fwd (args->workspace and
+   args->workspace_bytes are ignored, FDMA_FLAG_REUSE_CLASSIFICATION is ignored: every call
+   classifies).  Its workspace is one 16 MiB array of device memory compiled into the
+   library; every GPU that loads the library holds it until the process exits.  Problems
+   whose forward workspace (fdma_workspace_size(args, 0)) exceeds 16 MiB -- roughly more than
+   4095 tiles of 128 x 128 over B * Hkv -- are rejected with FDMA_ERR_WORKSPACE before
+   anything is launched.  No memory is allocated: no cudaMalloc, cudaFree or allocating
+   library call.  The first call on a device looks up the array's device address with that
+   device current; make that first call before any stream capture.  All calls share the one
+   array and each overwrites what the previous call left there (nothing in it needs to start
+   at zero), so calls whose executions overlap on the GPU race with each other: order them
+   on one stream or synchronize between them. */
+FDMA_API int fdma_fwd_noalloc(const fdma_args* args, void* out, float* lse, void* stream);
+
 /* Synchronizes `stream`, returns the first kernel-side error recorded since the last call
    (FDMA_OK if none) and clears it. */
 FDMA_API int fdma_get_device_error(void* stream);

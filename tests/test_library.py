@@ -31,7 +31,7 @@ def F():
 
 def test_header_declares_the_entry_points():
     assert _declared() == sorted(["fdma_workspace_size", "fdma_classify_blocks", "fdma_fwd", "fdma_bwd",
-                                  "fdma_get_device_error", "fdma_status_string"])
+                                  "fdma_get_device_error", "fdma_status_string", "fdma_fwd_noalloc"])
 
 
 def test_library_exports_every_declared_symbol(F):
