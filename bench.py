@@ -111,6 +111,26 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def replica_seed(base_seed: int, rank: int) -> int:
+    """Each replica draws its own copy of the workload (weak scaling)."""
+    return base_seed + rank
+
+
+def max_over_ranks(values, dist=None, device=None):
+    """Element-wise max of per-rank timings (the slowest rank sets the time)."""
+    import torch
+
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    if dist is not None and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_tflops(flops_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Aggregate throughput: the units all ranks processed / the (max) step time."""
+    return flops_per_rank * world / (ms_per_step * 1e-3) / 1e12
+
+
 def algorithmic_bytes(wl, bm):
     """Minimum bytes the path must move (mask once over causally allowed tiles,
     bias in fwd and bwd over active tiles, dBias over all of N^2, Q K V O dO dQ
@@ -146,7 +166,7 @@ def run_gpu(args):
     fdma.load()
     wl = W.WORKLOADS[WORKLOAD]
     dev = torch.device("cuda", local)
-    inp = W.make_inputs(wl, device=dev, seed=wl.seed + rank)
+    inp = W.make_inputs(wl, device=dev, seed=replica_seed(wl.seed, rank))
     q, k, v, do, bias, mask = (inp[n] for n in ("q", "k", "v", "dout", "bias", "mask"))
     a = fdma.make_args(q, k, v, mask=mask, bias=bias, causal=True, scale=wl.scale)
     wsp = fdma.alloc_workspace(a, True, dev)
@@ -239,17 +259,14 @@ def run_gpu(args):
     torch.cuda.synchronize()
     ms_e2e = s0.elapsed_time(s1) / e2e_steps
 
-    times = torch.tensor([ms_total, ms_e2e, ms_bwd, ms_fwd, ms_cls], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    ms_total, ms_e2e, ms_bwd, ms_fwd, ms_cls = times.tolist()
+    ms_total, ms_e2e, ms_bwd, ms_fwd, ms_cls = max_over_ranks([ms_total, ms_e2e, ms_bwd, ms_fwd, ms_cls], dist, dev)
     if rank != 0:
         dist.destroy_process_group()
         return None
 
     peaks = _peaks()
     ms_step = ms_total / args.steps
-    value = flops * ws / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(flops, ws, ms_step)
     bw = algorithmic_bytes(wl, bm.cpu().numpy())
     roof_ms = max(flops / (peaks["bf16_tflops_sustained"] * 1e12), bw["total"] / (peaks["hbm_gbs"] * 1e9)) * 1e3
     bwd_achieved = flops_bwd / (ms_bwd * 1e-3) / 1e12
@@ -280,7 +297,7 @@ def run_gpu(args):
                      "peak_source": peaks["source"] + " bf16_tflops_sustained",
                      "frac": round(bwd_achieved / peaks["bf16_tflops_sustained"], 4),
                      "traffic": None},
-        "e2e": {"value": round(flops * ws / (ms_e2e * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+        "e2e": {"value": round(whole_job_tflops(flops, ws, ms_e2e), 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3)},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clk.summary(),
