@@ -380,6 +380,387 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// ============================================================================
+// Two-head forward (used when the GQA group size is even).  One CTA = one
+// (batch, kv head, 128-row query tile, pair of query heads of the group):
+// both heads read the same K, V, bias and mask tiles, which are fetched once.
+// Warps: warpgroup 0 = {TMA producer, MMA issuer, 2 idle}, warpgroup 1 =
+// softmax of head 0, warpgroup 2 = softmax of head 1 (setmaxnreg moves
+// registers to the softmax groups).  The MMA issuer interleaves
+//   PV0_{n-1}, S0_n, PV1_{n-1}, S1_n
+// so each head's softmax overlaps the tensor-core work of the other head, and
+// S_w(n) (written over P_w(n-1)'s columns) completes only after PV_w(n-1):
+// the softmax may rescale O_w as soon as it sees S_w(n).
+// TMEM columns: S0/P0 0..127, S1/P1 128..255, O0 256.., O1 384...
+// Shared memory: Q0, Q1; K and V in one 3-slot ring (K_0, V_0, K_1, V_1, ...);
+// bias in a 2-slot ring.
+enum Fwd2Bar : int {
+  k2QFull = 0,
+  k2KvFull = 1,    // +slot (3)
+  k2KvEmpty = 4,   // +slot (3)
+  k2BFull = 7,     // +slot (2)
+  k2BEmpty = 9,    // +slot (2)
+  k2SFull = 11,    // +head (2)
+  k2PReady = 13,   // +head (2)
+  k2OFinal = 15,
+  k2Drain = 16,
+  kNumFwd2Bars = 17
+};
+
+constexpr int kFwd2Threads = 384;
+constexpr uint32_t kFwd2RegsLow = 104, kFwd2RegsHigh = 200;
+constexpr int kFwd2MinLaunchRegs = (kFwd2RegsLow + 2 * kFwd2RegsHigh) / 3;  // 168
+
+template <int D, bool HAS_BIAS>
+struct Fwd2Smem {
+  static constexpr uint32_t kQB = 128u * D * 2u;
+  static constexpr uint32_t kBB = 128u * 128u * 2u;
+  static constexpr uint32_t kOffQ = 0;                   // [2]
+  static constexpr uint32_t kOffKV = 2 * kQB;            // [3]
+  static constexpr uint32_t kOffBias = kOffKV + 3 * kQB; // [2]
+  static constexpr uint32_t kOffBar = kOffBias + (HAS_BIAS ? 2 * kBB : 0u);
+  static constexpr uint32_t kOffMap = kOffBar + kNumFwd2Bars * 8;
+  static constexpr uint32_t kOffMisc = kOffMap + kMaxKTiles;
+  static constexpr uint32_t kTotal = kOffMisc + 16;
+};
+
+template <int D, bool HAS_BIAS>
+__global__ void __launch_bounds__(kFwd2Threads, 1)
+    fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmB,
+                const FwdParams p) {
+  using L = Fwd2Smem<D, HAS_BIAS>;
+  constexpr int KB = D / 64;
+  constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
+  constexpr uint32_t IDESC_O = idesc_bf16(128, D, false, true);
+
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+  int8_t* map_row = reinterpret_cast<int8_t*>(smem + L::kOffMap);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int GP = p.G >> 1;  // head pairs per group
+  int id = blockIdx.x;
+  const int hp = id % GP;
+  id /= GP;
+  const int g = id % p.Hkv;
+  id /= p.Hkv;
+  const int b = id % p.B;
+  id /= p.B;
+  const int qt = p.nTq - 1 - id;  // longest causal rows first
+  const int h0 = g * p.G + 2 * hp;
+  const int q0 = qt * kTile;
+  const int64_t tile_base = (static_cast<int64_t>(b * p.Hkv + g) * p.nTq + qt) * p.nTk;
+  const bool ragged_k = (p.Nk & (kTile - 1)) != 0;
+
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicCAS(p.err, 0, kDevErrAlign);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumFwd2Bars; ++i) mbar_init(&bars[i], 1);
+    mbar_init(&bars[k2BEmpty + 0], 256);
+    mbar_init(&bars[k2BEmpty + 1], 256);
+    mbar_init(&bars[k2PReady + 0], 128);
+    mbar_init(&bars[k2PReady + 1], 128);
+    misc[1] = 0;
+    fence_mbar_init();
+  }
+  for (int kt = threadIdx.x; kt < p.nTk; kt += blockDim.x) map_row[kt] = p.kmap[tile_base + kt];
+  if (warp == 1) {
+    tmem_alloc(misc, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = misc[0];
+  const int first_kt = next_active(map_row, -1, p.nTk);
+  const bool any_active = first_kt < p.nTk;
+
+  uint8_t* sQ = smem + L::kOffQ;
+  uint8_t* sKV = smem + L::kOffKV;
+  uint8_t* sB = smem + L::kOffBias;
+
+  if (warp < 4) {
+    regs_decrease<kFwd2RegsLow>();
+    if (warp == 0 && lane == 0 && any_active) {
+      // ---------------------------------------------------------------- producer
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      if (HAS_BIAS) tma_prefetch_desc(&tmB);
+      mbar_arrive_expect_tx(&bars[k2QFull], 2 * L::kQB);
+#pragma unroll
+      for (int w = 0; w < 2; ++w)
+#pragma unroll
+        for (int c = 0; c < KB; ++c)
+          tma_load_4d(sQ + w * L::kQB + c * 16384, &tmQ, &bars[k2QFull], c * 64, q0, h0 + w, b);
+      int n = 0, items = 0;
+      bool ok = true;
+      for (int kt = first_kt; ok && kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
+        const int k0 = kt * kTile;
+        // K_n
+        {
+          const int it = 2 * n, sl = it % 3;
+          if (!(ok = mbar_wait(&bars[k2KvEmpty + sl], ((it / 3) & 1) ^ 1, p.err, kDevErrTimeout, abort_flag))) break;
+          mbar_arrive_expect_tx(&bars[k2KvFull + sl], L::kQB);
+#pragma unroll
+          for (int c = 0; c < KB; ++c)
+            tma_load_4d(sKV + sl * L::kQB + c * 16384, &tmK, &bars[k2KvFull + sl], c * 64, k0, g, b);
+          items = it + 1;
+        }
+        if (HAS_BIAS) {
+          const int sb = n & 1;
+          if (!(ok = mbar_wait(&bars[k2BEmpty + sb], ((n >> 1) & 1) ^ 1, p.err, kDevErrTimeout, abort_flag))) break;
+          mbar_arrive_expect_tx(&bars[k2BFull + sb], L::kBB);
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            tma_load_4d(sB + sb * L::kBB + c * 16384, &tmB, &bars[k2BFull + sb], k0 + c * 64, q0, g, b);
+        }
+        // V_n
+        {
+          const int it = 2 * n + 1, sl = it % 3;
+          if (!(ok = mbar_wait(&bars[k2KvEmpty + sl], ((it / 3) & 1) ^ 1, p.err, kDevErrTimeout, abort_flag))) break;
+          mbar_arrive_expect_tx(&bars[k2KvFull + sl], L::kQB);
+#pragma unroll
+          for (int c = 0; c < KB; ++c)
+            tma_load_4d(sKV + sl * L::kQB + c * 16384, &tmV, &bars[k2KvFull + sl], c * 64, k0, g, b);
+          items = it + 1;
+        }
+      }
+      if (*abort_flag) {
+        mbar_wait(&bars[k2QFull], 0, p.err, kDevErrTimeout, nullptr);
+        for (int it = items > 3 ? items - 3 : 0; it < items; ++it)
+          mbar_wait(&bars[k2KvFull + it % 3], (it / 3) & 1, p.err, kDevErrTimeout, nullptr);
+      }
+    } else if (warp == 1 && lane == 0 && any_active) {
+      // ---------------------------------------------------------------- MMA issuer
+      bool ok = mbar_wait(&bars[k2QFull], 0, p.err, kDevErrTimeout, abort_flag);
+      tc_fence_after();
+      const uint64_t qdesc0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t qdesc1 = sdesc_sw128(smem_u32(sQ + L::kQB), 16, 1024);
+      const uint64_t kvk0 = sdesc_sw128(smem_u32(sKV), 16, 1024);       // K-major view of slot 0
+      const uint64_t kvmn0 = sdesc_sw128(smem_u32(sKV), 16384, 1024);   // MN-major view of slot 0
+      const uint64_t slot_step = static_cast<uint64_t>(L::kQB >> 4);
+      auto issue_s = [&](int w, int n) {
+        const int sl = (2 * n) % 3;
+        const uint64_t kd = kvk0 + sl * slot_step;
+        const uint64_t qd = w == 0 ? qdesc0 : qdesc1;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          umma_ss(tbase + w * 128, qd + kmajor_step(k, 128), kd + kmajor_step(k, 128), IDESC_S, k > 0);
+        umma_commit(&bars[k2SFull + w]);
+      };
+      auto issue_pv = [&](int w, int m) {
+        const int sl = (2 * m + 1) % 3;
+        const uint64_t vd = kvmn0 + sl * slot_step;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          umma_ts(tbase + 256 + w * 128, tbase + w * 128 + k * 8, vd + static_cast<uint64_t>((k * 2048) >> 4),
+                  IDESC_O, (m > 0 || k > 0) ? 1u : 0u);
+      };
+      int n = 0;
+      for (int kt = first_kt; ok && kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
+        const int itk = 2 * n;
+        if (!(ok = mbar_wait(&bars[k2KvFull + itk % 3], (itk / 3) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        tc_fence_after();
+        if (n == 0) {
+          issue_s(0, 0);
+          issue_s(1, 0);
+          umma_commit(&bars[k2KvEmpty + itk % 3]);
+          continue;
+        }
+        const int m = n - 1, itv = 2 * m + 1;
+        if (!(ok = mbar_wait(&bars[k2KvFull + itv % 3], (itv / 3) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        if (!(ok = mbar_wait(&bars[k2PReady + 0], m & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        tc_fence_after();
+        issue_pv(0, m);
+        issue_s(0, n);
+        if (!(ok = mbar_wait(&bars[k2PReady + 1], m & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        tc_fence_after();
+        issue_pv(1, m);
+        umma_commit(&bars[k2KvEmpty + itv % 3]);
+        issue_s(1, n);
+        umma_commit(&bars[k2KvEmpty + itk % 3]);
+      }
+      if (ok && n > 0) {
+        const int m = n - 1, itv = 2 * m + 1;
+        ok = mbar_wait(&bars[k2KvFull + itv % 3], (itv / 3) & 1, p.err, kDevErrTimeout, abort_flag) &&
+             mbar_wait(&bars[k2PReady + 0], m & 1, p.err, kDevErrTimeout, abort_flag);
+        if (ok) {
+          tc_fence_after();
+          issue_pv(0, m);
+          ok = mbar_wait(&bars[k2PReady + 1], m & 1, p.err, kDevErrTimeout, abort_flag);
+          if (ok) {
+            tc_fence_after();
+            issue_pv(1, m);
+            umma_commit(&bars[k2KvEmpty + itv % 3]);
+          }
+        }
+      }
+      umma_commit(&bars[k2OFinal]);
+      umma_commit(&bars[k2Drain]);
+      mbar_wait(&bars[k2Drain], 0, p.err, kDevErrTimeout, nullptr);
+    }
+  } else {
+    regs_increase<kFwd2RegsHigh>();
+    // ------------------------------------------------------------------ softmax
+    const int w = (warp >> 2) - 1;  // head within the pair
+    const int h = h0 + w;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int i = q0 + r;
+    const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t scol = w * 128, ocol = 256 + w * 128;
+    float m_ref = kNegInf, l = 0.f;
+    int n = 0;
+    bool ok = true;
+    uint32_t raw[32];
+    for (int kt = first_kt; kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
+      if (!(ok = mbar_wait(&bars[k2SFull + w], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
+      tc_fence_after();
+      const bool partial = map_row[kt] == kPartial || (ragged_k && kt == p.nTk - 1);
+      uint4 bits = make_uint4(~0u, ~0u, ~0u, ~0u);
+      if (partial) bits = __ldg(&p.bits_row[(tile_base + kt) * kTile + r]);
+      float x[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(tl + scol + c * 32, raw);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[c * 32 + j] = __uint_as_float(raw[j]) * p.scale_log2;
+      }
+      if (HAS_BIAS) {
+        const int sb = n & 1;
+        if (!(ok = mbar_wait(&bars[k2BFull + sb], (n >> 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        const uint8_t* bt = sB + sb * L::kBB + r * 128;
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) {
+          const uint4 v = *reinterpret_cast<const uint4*>(bt + (cc >> 3) * 16384 + (((cc & 7) ^ (r & 7)) << 4));
+          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            x[cc * 8 + 2 * e] = fmaf(__uint_as_float(wv[e] << 16), kLog2e, x[cc * 8 + 2 * e]);
+            x[cc * 8 + 2 * e + 1] = fmaf(__uint_as_float(wv[e] & 0xFFFF0000u), kLog2e, x[cc * 8 + 2 * e + 1]);
+          }
+        }
+        mbar_arrive(&bars[k2BEmpty + sb]);
+      }
+      if (partial) {
+        const uint32_t bw[4] = {bits.x, bits.y, bits.z, bits.w};
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (!((bw[c >> 5] >> (c & 31)) & 1u)) x[c] = kNegInf;
+      }
+      float mx8[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) mx8[t] = x[t];
+#pragma unroll
+      for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float m_new = fmaxf(m_ref, mx);
+      float alpha = 1.f;
+      bool resc = false;
+      if (m_new > m_ref + kRescaleThreshold) {
+        if (m_ref == kNegInf) {
+          m_ref = m_new;
+        } else {
+          alpha = ex2(m_ref - m_new);
+          l *= alpha;
+          m_ref = m_new;
+          resc = true;
+        }
+      }
+      const float mu = (m_ref == kNegInf) ? 0.f : m_ref;
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float p0 = ex2(x[c * 32 + 2 * j] - mu);
+          const float p1 = ex2(x[c * 32 + 2 * j + 1] - mu);
+          pk[j] = pack_bf16x2(p0, p1);
+          sum4[j & 3] += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xFFFF0000u);
+        }
+        tmem_st16(tl + scol + c * 16, pk);
+      }
+      l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      if (__any_sync(0xffffffffu, resc)) {
+        // S_w(n) was issued after PV_w(n-1), so O_w is complete here; PV_w(n) is
+        // issued only after the arrival below.
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t o16[16];
+          tmem_ld16(tl + ocol + c * 16, o16);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) o16[j] = __float_as_uint(__uint_as_float(o16[j]) * alpha);
+          tmem_st16(tl + ocol + c * 16, o16);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars[k2PReady + w]);
+    }
+    // ------------------------------------------------------------------ epilogue
+    if (ok && n > 0) ok = mbar_wait(&bars[k2OFinal], 0, p.err, kDevErrTimeout, abort_flag);
+    if (ok) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint16_t* orow = p.out + ((static_cast<int64_t>(b) * p.Nq + i) * p.Hq + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        if (n > 0) {
+          tmem_ld32(tl + ocol + c * 32, raw);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) raw[j] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          pk[j] = pack_bf16x2(__uint_as_float(raw[2 * j]) * inv, __uint_as_float(raw[2 * j + 1]) * inv);
+        if (i < p.Nq) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+      if (i < p.Nq)
+        p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + i] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : kNegInf;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D, bool HB>
+cudaError_t launch_fwd2_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tb,
+                          const FwdParams& p, cudaStream_t stream) {
+  using L = Fwd2Smem<D, HB>;
+  auto kern = fwd2_kernel<D, HB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs < kFwd2MinLaunchRegs) return cudaErrorInvalidConfiguration;  // setmaxnreg split must fit
+  const unsigned grid = static_cast<unsigned>(p.B) * p.Hkv * (p.G / 2) * p.nTq;
+  kern<<<grid, kFwd2Threads, L::kTotal, stream>>>(tq, tk, tv, tb, p);
+  return cudaGetLastError();
+}
+
 template <int D, bool HB>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tb,
                          const FwdParams& p, cudaStream_t stream) {
@@ -396,6 +777,12 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 cudaError_t launch_fwd(int d, bool has_bias, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tb, const FwdParams& p, cudaStream_t stream) {
+  if (p.G % 2 == 0) {
+    if (d == 128) return has_bias ? launch_fwd2_t<128, true>(tq, tk, tv, tb, p, stream)
+                                  : launch_fwd2_t<128, false>(tq, tk, tv, tb, p, stream);
+    if (d == 64) return has_bias ? launch_fwd2_t<64, true>(tq, tk, tv, tb, p, stream)
+                                 : launch_fwd2_t<64, false>(tq, tk, tv, tb, p, stream);
+  }
   if (d == 128) return has_bias ? launch_fwd_t<128, true>(tq, tk, tv, tb, p, stream)
                                 : launch_fwd_t<128, false>(tq, tk, tv, tb, p, stream);
   if (d == 64) return has_bias ? launch_fwd_t<64, true>(tq, tk, tv, tb, p, stream)
