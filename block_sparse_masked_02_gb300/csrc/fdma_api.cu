@@ -310,7 +310,25 @@ int fdma_bwd(const fdma_args* a, const void* out, const void* dout, const float*
   p.dv = static_cast<uint16_t*>(dv);
   p.dbias = static_cast<uint16_t*>(dbias);
   p.err = err;
-  if (launch_bwd(a->d, a->bias != nullptr, dbias != nullptr, tq, tk, tv, tdo, p, stream) != cudaSuccess)
+  CUtensorMap tb = tq;
+  if (a->bias != nullptr) {
+    const uint64_t dims[4] = {static_cast<uint64_t>(a->Nk), static_cast<uint64_t>(a->Nq),
+                              static_cast<uint64_t>(a->Hkv), static_cast<uint64_t>(a->B)};
+    const uint64_t sb[3] = {static_cast<uint64_t>(a->bias_stride[2]) * 2, static_cast<uint64_t>(a->bias_stride[1]) * 2,
+                            static_cast<uint64_t>(a->bias_stride[0]) * 2};
+    if ((a->B > 1 && a->bias_stride[0] == 0) || (a->Hkv > 1 && a->bias_stride[1] == 0) || a->bias_stride[2] == 0)
+      return FDMA_ERR_UNSUPPORTED;
+    if (!make_map(&tb, a->bias, dims, sb)) return FDMA_ERR_UNSUPPORTED;
+  }
+  CUtensorMap tdb = tq;
+  if (dbias != nullptr) {
+    const uint64_t dims[4] = {static_cast<uint64_t>(a->Nk), static_cast<uint64_t>(a->Nq),
+                              static_cast<uint64_t>(a->Hkv), static_cast<uint64_t>(a->B)};
+    const uint64_t sb[3] = {static_cast<uint64_t>(a->Nk) * 2, static_cast<uint64_t>(a->Nq) * a->Nk * 2,
+                            static_cast<uint64_t>(a->Hkv) * a->Nq * a->Nk * 2};
+    if (!make_map(&tdb, dbias, dims, sb)) return FDMA_ERR_UNSUPPORTED;
+  }
+  if (launch_bwd(a->d, a->bias != nullptr, dbias != nullptr, tq, tk, tv, tdo, tb, tdb, p, stream) != cudaSuccess)
     return FDMA_ERR_CUDA;
   DqConvertParams cp{};
   cp.B = a->B;

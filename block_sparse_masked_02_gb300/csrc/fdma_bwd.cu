@@ -15,13 +15,16 @@
 //                      dS^T = P^T (dP^T - delta)
 //                      dV  += P^T dO          (TS: P^T packed in TMEM cols 0..31, 64..95)
 //                      dK  += dS^T Q          (SS: dS^T staged in smem)
-//                      dQ   = dS K            (SS, reuses TMEM cols 128..)
-//                    dQ is added to an fp32 accumulator with vector
-//                    reductions; dBias = sum over the group's heads of dS is
+//                      dQ   = dS K            (SS, reuses TMEM cols 128..; for
+//                                              d = 128 computed as dQ^T = K^T dS^T so
+//                                              that each warp's reduction covers 32
+//                                              consecutive floats of one row)
+//                    dQ is added to an fp32 accumulator with reductions; dBias = sum over the group's heads of dS is
 //                    kept in registers (one thread per key and half of the
 //                    query tile) and written once per (query tile, key tile);
-//                    the bias^T slice is loaded once per query tile for all
-//                    heads; skipped tiles of dBias are written as zeros by the
+//                    the bias tile of a query tile is TMA-loaded into shared
+//                    memory once and each thread copies its key column into
+//                    registers for all heads; skipped tiles of dBias are written as zeros by the
 //                    same CTA.  Warps: 0 TMA, 1 MMA, 4..11 two compute groups.
 //   dq_convert       fp32 accumulator -> bf16 dQ.
 #include "fdma_internal.h"
@@ -94,34 +97,42 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const DqConvertParams p
 // ----------------------------------------------------------------------- main backward
 enum BwdBar : int {
   kKVFull = 0,
-  kQdoFull = 1,   // +slot
-  kQdoEmpty = 3,  // +slot
-  kSFull = 5,
-  kDpFull = 6,
-  kPReady = 7,
-  kDqFull = 8,
-  kDqFree = 9,
-  kDsFree = 10,
-  kFinal = 11,
-  kDrain = 12,
-  kNumBwdBars = 13
+  kQFull = 1,    // +slot (2): Q, lse2, delta of one step
+  kQEmpty = 3,   // +slot (2)
+  kDoFull = 5,   // +slot (up to 2)
+  kDoEmpty = 7,  // +slot (up to 2)
+  kBFull = 9,    // bias tile of the current query tile
+  kBEmpty = 10,
+  kSFull = 11,
+  kDpFull = 12,
+  kPReady = 13,
+  kDqFull = 14,
+  kDqFree = 15,
+  kDsFree = 16,
+  kFinal = 17,
+  kDrain = 18,
+  kNumBwdBars = 19
 };
 
 // 12 warps: warpgroup 0 = {TMA producer, MMA issuer, 2 idle}, warpgroups 1-2 = compute.
 constexpr int kBwdThreads = 384;
-constexpr uint32_t kRegsLow = 104, kRegsHigh = 200;
+constexpr uint32_t kRegsLow = 120, kRegsHigh = 192;
 constexpr int kBwdMinLaunchRegs = (kRegsLow + 2 * kRegsHigh) / 3;  // 168
 
-template <int D>
+// Shared memory: K, V resident; Q (+ lse, delta) in 2 slots; dO in 1 slot when a
+// bias tile needs the room, else 2; bias tile (one query tile, 32 KB); dS^T.
+template <int D, bool HAS_BIAS>
 struct BwdSmem {
   static constexpr uint32_t kQB = 128u * D * 2u;
+  static constexpr int kDoStages = HAS_BIAS ? 1 : 2;
   static constexpr uint32_t kOffK = 0;
   static constexpr uint32_t kOffV = kQB;
-  static constexpr uint32_t kOffQ = 2 * kQB;    // [2]
-  static constexpr uint32_t kOffDO = 4 * kQB;   // [2]
-  static constexpr uint32_t kOffDS = 6 * kQB;   // 128 keys x 128 queries bf16
-  static constexpr uint32_t kOffLse = kOffDS + 32768;   // [2][128] f32
-  static constexpr uint32_t kOffDelta = kOffLse + 1024; // [2][128] f32
+  static constexpr uint32_t kOffQ = 2 * kQB;                      // [2]
+  static constexpr uint32_t kOffDO = 4 * kQB;                     // [kDoStages]
+  static constexpr uint32_t kOffBias = kOffDO + kDoStages * kQB;  // 128 x 128 bf16 (if HAS_BIAS)
+  static constexpr uint32_t kOffDS = kOffBias + (HAS_BIAS ? 32768u : 0u);  // 128 keys x 128 queries bf16
+  static constexpr uint32_t kOffLse = kOffDS + 32768;    // [2][128] f32
+  static constexpr uint32_t kOffDelta = kOffLse + 1024;  // [2][128] f32
   static constexpr uint32_t kOffBar = kOffDelta + 1024;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBwdBars * 8;
   static constexpr uint32_t kTotal = kOffMisc + 16;
@@ -144,17 +155,25 @@ struct ColIter {
   }
 };
 
+__device__ __forceinline__ void red_add_f32(float* gptr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(gptr), "f"(v) : "memory");
+}
+
 template <int D, bool HAS_BIAS, bool WANT_DBIAS>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+               const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmDB,
                const BwdParams p) {
-  using L = BwdSmem<D>;
+  using L = BwdSmem<D, HAS_BIAS>;
   constexpr int KB = D / 64;
+  constexpr int DOS = L::kDoStages;
+  constexpr bool DQ_T = (D == 128);  // dQ^T = K^T dS^T (lane = head-dim index) for coalesced reductions
   constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);   // S^T, dP^T
   constexpr uint32_t IDESC_DV = idesc_bf16(128, D, false, true);     // P^T(tmem) x dO (N contiguous)
   constexpr uint32_t IDESC_DK = idesc_bf16(128, D, false, true);     // dS^T(K-major) x Q (N contiguous)
-  constexpr uint32_t IDESC_DQ = idesc_bf16(128, D, true, true);      // dS (M contiguous) x K (N contiguous)
+  constexpr uint32_t IDESC_DQ = DQ_T ? idesc_bf16(128, 128, true, true)   // K^T (M=d contiguous) x dS^T
+                                     : idesc_bf16(128, D, true, true);    // dS (M contiguous) x K
 
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
@@ -164,6 +183,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sV = smem + L::kOffV;
   uint8_t* sQ = smem + L::kOffQ;
   uint8_t* sDO = smem + L::kOffDO;
+  uint8_t* sBias = smem + L::kOffBias;
   uint8_t* sDS = smem + L::kOffDS;
   float* sLse = reinterpret_cast<float*>(smem + L::kOffLse);
   float* sDelta = reinterpret_cast<float*>(smem + L::kOffDelta);
@@ -188,6 +208,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int i = 0; i < kNumBwdBars; ++i) mbar_init(&bars[i], 1);
     mbar_init(&bars[kPReady], 256);
     mbar_init(&bars[kDqFree], 256);
+    mbar_init(&bars[kBEmpty], 256);
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -204,109 +225,128 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp < 4) {
    regs_decrease<kRegsLow>();
-   if (warp == 0) {
+   if (warp == 0 && lane == 0 && any_active) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && any_active) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      tma_prefetch_desc(&tmDO);
-      mbar_arrive_expect_tx(&bars[kKVFull], 2 * L::kQB);
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmDO);
+    if (HAS_BIAS) tma_prefetch_desc(&tmB);
+    mbar_arrive_expect_tx(&bars[kKVFull], 2 * L::kQB);
 #pragma unroll
-      for (int c = 0; c < KB; ++c) {
-        tma_load_4d(sK + c * 16384, &tmK, &bars[kKVFull], c * 64, k0, g, b);
-        tma_load_4d(sV + c * 16384, &tmV, &bars[kKVFull], c * 64, k0, g, b);
-      }
-      int n = 0, issued = 0;
-      bool ok = true;
-      for (int qt = first_qt; ok && qt < p.nTq; qt = it.next(qt)) {
-        for (int hh = 0; hh < p.G; ++hh, ++n) {
-          const int h = g * p.G + hh;
-          const int s = n & 1;
-          if (!(ok = mbar_wait(&bars[kQdoEmpty + s], ((n >> 1) & 1) ^ 1, p.err, kDevErrTimeout, abort_flag))) break;
-          mbar_arrive_expect_tx(&bars[kQdoFull + s], 2 * L::kQB + 1024);
+    for (int c = 0; c < KB; ++c) {
+      tma_load_4d(sK + c * 16384, &tmK, &bars[kKVFull], c * 64, k0, g, b);
+      tma_load_4d(sV + c * 16384, &tmV, &bars[kKVFull], c * 64, k0, g, b);
+    }
+    int n = 0, qi_count = 0;
+    bool ok = true;
+    for (int qt = first_qt; ok && qt < p.nTq; qt = it.next(qt), ++qi_count) {
+      if (HAS_BIAS) {
+        if (!(ok = mbar_wait(&bars[kBEmpty], (qi_count & 1) ^ 1, p.err, kDevErrTimeout, abort_flag))) break;
+        mbar_arrive_expect_tx(&bars[kBFull], 32768);
 #pragma unroll
-          for (int c = 0; c < KB; ++c) {
-            tma_load_4d(sQ + s * L::kQB + c * 16384, &tmQ, &bars[kQdoFull + s], c * 64, qt * kTile, h, b);
-            tma_load_4d(sDO + s * L::kQB + c * 16384, &tmDO, &bars[kQdoFull + s], c * 64, qt * kTile, h, b);
-          }
-          const int64_t vec = (static_cast<int64_t>(b) * p.Hq + h) * p.nqpad + qt * kTile;
-          bulk_load(sLse + s * 128, p.lse2 + vec, 512, &bars[kQdoFull + s]);
-          bulk_load(sDelta + s * 128, p.delta + vec, 512, &bars[kQdoFull + s]);
-          issued = n + 1;
-        }
+        for (int c = 0; c < 2; ++c) tma_load_4d(sBias + c * 16384, &tmB, &bars[kBFull], k0 + c * 64, qt * kTile, g, b);
       }
-      if (*abort_flag) {
-        mbar_wait(&bars[kKVFull], 0, p.err, kDevErrTimeout, nullptr);
-        for (int m = issued > 2 ? issued - 2 : 0; m < issued; ++m)
-          mbar_wait(&bars[kQdoFull + (m & 1)], (m >> 1) & 1, p.err, kDevErrTimeout, nullptr);
+      for (int hh = 0; hh < p.G; ++hh, ++n) {
+        const int h = g * p.G + hh;
+        const int s = n & 1;
+        if (!(ok = mbar_wait(&bars[kQEmpty + s], ((n >> 1) & 1) ^ 1, p.err, kDevErrTimeout, abort_flag))) break;
+        mbar_arrive_expect_tx(&bars[kQFull + s], L::kQB + 1024);
+#pragma unroll
+        for (int c = 0; c < KB; ++c)
+          tma_load_4d(sQ + s * L::kQB + c * 16384, &tmQ, &bars[kQFull + s], c * 64, qt * kTile, h, b);
+        const int64_t vec = (static_cast<int64_t>(b) * p.Hq + h) * p.nqpad + qt * kTile;
+        bulk_load(sLse + s * 128, p.lse2 + vec, 512, &bars[kQFull + s]);
+        bulk_load(sDelta + s * 128, p.delta + vec, 512, &bars[kQFull + s]);
+        const int sd = n % DOS;
+        if (!(ok = mbar_wait(&bars[kDoEmpty + sd], ((n / DOS) & 1) ^ 1, p.err, kDevErrTimeout, abort_flag))) break;
+        mbar_arrive_expect_tx(&bars[kDoFull + sd], L::kQB);
+#pragma unroll
+        for (int c = 0; c < KB; ++c)
+          tma_load_4d(sDO + sd * L::kQB + c * 16384, &tmDO, &bars[kDoFull + sd], c * 64, qt * kTile, h, b);
       }
     }
-  } else if (warp == 1) {
+    if (*abort_flag) {
+      // let this CTA's own copies land before it retires (bounded waits)
+      mbar_wait(&bars[kKVFull], 0, p.err, kDevErrTimeout, nullptr);
+      for (int m = n > 2 ? n - 2 : 0; m <= n; ++m) {
+        mbar_wait(&bars[kQFull + (m & 1)], (m >> 1) & 1, p.err, kDevErrTimeout, nullptr);
+        mbar_wait(&bars[kDoFull + m % DOS], (m / DOS) & 1, p.err, kDevErrTimeout, nullptr);
+      }
+      if (HAS_BIAS && qi_count > 0) mbar_wait(&bars[kBFull], (qi_count - 1) & 1, p.err, kDevErrTimeout, nullptr);
+    }
+   } else if (warp == 1 && lane == 0 && any_active) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && any_active) {
-      bool ok = mbar_wait(&bars[kKVFull], 0, p.err, kDevErrTimeout, abort_flag);
-      tc_fence_after();
-      const uint64_t kdesc_k = sdesc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t vdesc_k = sdesc_sw128(smem_u32(sV), 16, 1024);
-      const uint64_t kdesc_mn = sdesc_sw128(smem_u32(sK), 16384, 1024);
-      const uint64_t dsdesc_k = sdesc_sw128(smem_u32(sDS), 16, 1024);
-      const uint64_t dsdesc_mn = sdesc_sw128(smem_u32(sDS), 16384, 1024);
-      int n = 0;
-      for (int qt = first_qt; ok && qt < p.nTq; qt = it.next(qt)) {
-        for (int hh = 0; hh < p.G; ++hh, ++n) {
-          const int s = n & 1;
-          if (!(ok = mbar_wait(&bars[kQdoFull + s], (n >> 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
-          tc_fence_after();
-          const uint64_t qdesc_k = sdesc_sw128(smem_u32(sQ + s * L::kQB), 16, 1024);
-          const uint64_t qdesc_mn = sdesc_sw128(smem_u32(sQ + s * L::kQB), 16384, 1024);
-          const uint64_t dodesc_k = sdesc_sw128(smem_u32(sDO + s * L::kQB), 16, 1024);
-          const uint64_t dodesc_mn = sdesc_sw128(smem_u32(sDO + s * L::kQB), 16384, 1024);
-          // S^T = K Q^T
+    bool ok = mbar_wait(&bars[kKVFull], 0, p.err, kDevErrTimeout, abort_flag);
+    tc_fence_after();
+    const uint64_t kdesc_k = sdesc_sw128(smem_u32(sK), 16, 1024);
+    const uint64_t vdesc_k = sdesc_sw128(smem_u32(sV), 16, 1024);
+    const uint64_t kdesc_mn = sdesc_sw128(smem_u32(sK), 16384, 1024);
+    const uint64_t dsdesc_k = sdesc_sw128(smem_u32(sDS), 16, 1024);
+    const uint64_t dsdesc_mn = sdesc_sw128(smem_u32(sDS), 16384, 1024);
+    const uint64_t q0desc_k = sdesc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t q0desc_mn = sdesc_sw128(smem_u32(sQ), 16384, 1024);
+    const uint64_t do0desc_k = sdesc_sw128(smem_u32(sDO), 16, 1024);
+    const uint64_t do0desc_mn = sdesc_sw128(smem_u32(sDO), 16384, 1024);
+    const uint64_t slot = static_cast<uint64_t>(L::kQB >> 4);
+    int n = 0;
+    for (int qt = first_qt; ok && qt < p.nTq; qt = it.next(qt)) {
+      for (int hh = 0; hh < p.G; ++hh, ++n) {
+        const int s = n & 1, sd = n % DOS;
+        if (!(ok = mbar_wait(&bars[kQFull + s], (n >> 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        tc_fence_after();
+        const uint64_t qdesc_k = q0desc_k + s * slot, qdesc_mn = q0desc_mn + s * slot;
+        const uint64_t dodesc_k = do0desc_k + sd * slot, dodesc_mn = do0desc_mn + sd * slot;
+        // S^T = K Q^T
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            umma_ss(tbase, kdesc_k + kmajor_step(k, 128), qdesc_k + kmajor_step(k, 128), IDESC_S, k > 0);
-          umma_commit(&bars[kSFull]);
-          // dP^T = V dO^T into the columns the previous dQ used
-          if (n > 0) {
-            if (!(ok = mbar_wait(&bars[kDqFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
-            tc_fence_after();
-          }
+        for (int k = 0; k < D / 16; ++k)
+          umma_ss(tbase, kdesc_k + kmajor_step(k, 128), qdesc_k + kmajor_step(k, 128), IDESC_S, k > 0);
+        umma_commit(&bars[kSFull]);
+        // dP^T = V dO^T into the columns the previous dQ used
+        if (!(ok = mbar_wait(&bars[kDoFull + sd], (n / DOS) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        if (n > 0 && !(ok = mbar_wait(&bars[kDqFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            umma_ss(tbase + 128, vdesc_k + kmajor_step(k, 128), dodesc_k + kmajor_step(k, 128), IDESC_S, k > 0);
-          umma_commit(&bars[kDpFull]);
-          if (!(ok = mbar_wait(&bars[kPReady], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
-          tc_fence_after();
-          // dV += P^T dO ; dK += dS^T Q   (K dimension = 128 queries)
+        for (int k = 0; k < D / 16; ++k)
+          umma_ss(tbase + 128, vdesc_k + kmajor_step(k, 128), dodesc_k + kmajor_step(k, 128), IDESC_S, k > 0);
+        umma_commit(&bars[kDpFull]);
+        if (!(ok = mbar_wait(&bars[kPReady], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        tc_fence_after();
+        // dV += P^T dO  (K dimension = 128 queries; P^T packed in TMEM cols 0..31 and 64..95)
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            umma_ts(tbase + 256, tbase + k * 8 + (k >= 4 ? 32 : 0), dodesc_mn + mnmajor_step(k), IDESC_DV,
-                    (n > 0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < 8; ++k)
+          umma_ts(tbase + 256, tbase + k * 8 + (k >= 4 ? 32 : 0), dodesc_mn + mnmajor_step(k), IDESC_DV,
+                  (n > 0 || k > 0) ? 1u : 0u);
+        umma_commit(&bars[kDoEmpty + sd]);
+        // dK += dS^T Q
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            umma_ss(tbase + 384, dsdesc_k + kmajor_step(k, 128), qdesc_mn + mnmajor_step(k), IDESC_DK,
-                    (n > 0 || k > 0) ? 1u : 0u);
-          umma_commit(&bars[kQdoEmpty + s]);
-          // dQ = dS K   (K dimension = 128 keys)
+        for (int k = 0; k < 8; ++k)
+          umma_ss(tbase + 384, dsdesc_k + kmajor_step(k, 128), qdesc_mn + mnmajor_step(k), IDESC_DK,
+                  (n > 0 || k > 0) ? 1u : 0u);
+        umma_commit(&bars[kQEmpty + s]);
+        // dQ (K dimension = 128 keys)
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
+        for (int k = 0; k < 8; ++k) {
+          if (DQ_T)
+            umma_ss(tbase + 128, kdesc_mn + mnmajor_step(k), dsdesc_mn + mnmajor_step(k), IDESC_DQ, k > 0);
+          else
             umma_ss(tbase + 128, dsdesc_mn + mnmajor_step(k), kdesc_mn + mnmajor_step(k), IDESC_DQ, k > 0);
-          umma_commit(&bars[kDqFull]);
-          umma_commit(&bars[kDsFree]);
         }
+        umma_commit(&bars[kDqFull]);
+        umma_commit(&bars[kDsFree]);
       }
-      umma_commit(&bars[kFinal]);
-      umma_commit(&bars[kDrain]);
-      mbar_wait(&bars[kDrain], 0, p.err, kDevErrTimeout, nullptr);
     }
+    umma_commit(&bars[kFinal]);
+    umma_commit(&bars[kDrain]);
+    mbar_wait(&bars[kDrain], 0, p.err, kDevErrTimeout, nullptr);
    }
   } else {
    regs_increase<kRegsHigh>();
    {
     // ------------------------------------------------------------ compute
     // Two warpgroups: wg 0 owns queries 0..63 of every step, wg 1 queries 64..127.
-    // Thread (quad, lane) owns key row j of S^T/dP^T/dK/dV and query row j of dQ.
+    // Thread (quad, lane) owns key row j of S^T/dP^T/dK/dV, and row j of the dQ
+    // accumulator in TMEM (head-dim index j for d = 128, query row j for d = 64).
     const int wg = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int j = quad * 32 + lane;
@@ -318,9 +358,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     float acc[WANT_DBIAS ? 64 : 1];
 #pragma unroll
     for (int c = 0; c < (WANT_DBIAS ? 64 : 1); ++c) acc[c] = 0.f;
-    int n = 0;
+    int n = 0, qi_count = 0;
     bool ok = true;
-    for (int qt = first_qt; ok && qt < p.nTq; qt = it.next(qt)) {
+    for (int qt = first_qt; ok && qt < p.nTq; qt = it.next(qt), ++qi_count) {
       const int q0 = qt * kTile;
       const int64_t tile = col_base + static_cast<int64_t>(qt) * p.nTk;
       const bool partial = p.kmap[tile] == kPartial || ragged_k || (ragged_q_any && qt == p.nTq - 1);
@@ -331,29 +371,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bw1 = bb.y;
       }
       const int rows_in = min(kTile, p.Nq - q0) - qbase;  // valid queries in this half
-      // bias^T column slice, loaded once per query tile and reused by every head of the group
+      // bias^T column slice of this query tile, copied once into registers for every head
       uint32_t bpk[HAS_BIAS ? 32 : 1];
       if (HAS_BIAS) {
-        const uint16_t* bcol = p.bias + b * p.bs_b + g * p.bs_h + static_cast<int64_t>(q0 + qbase) * p.bs_r + kidx;
+        if (!(ok = mbar_wait(&bars[kBFull], qi_count & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        const uint8_t* bt = sBias + (j >> 6) * 16384 + (j & 7) * 2;
+        const int jc = (j & 63) >> 3;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint16_t braw[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int qi = half * 32 + e;
-            braw[e] = (kin && qi < rows_in) ? __ldg(bcol + static_cast<int64_t>(qi) * p.bs_r) : static_cast<uint16_t>(0);
-          }
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            bpk[half * 16 + e] = static_cast<uint32_t>(braw[2 * e]) | (static_cast<uint32_t>(braw[2 * e + 1]) << 16);
+        for (int e = 0; e < 32; ++e) {
+          const int i0 = qbase + 2 * e, i1 = i0 + 1;
+          const uint32_t lo = *reinterpret_cast<const uint16_t*>(bt + i0 * 128 + ((jc ^ (i0 & 7)) << 4));
+          const uint32_t hi = *reinterpret_cast<const uint16_t*>(bt + i1 * 128 + ((jc ^ (i1 & 7)) << 4));
+          bpk[e] = lo | (hi << 16);
         }
+        mbar_arrive(&bars[kBEmpty]);
       }
       for (int hh = 0; hh < p.G; ++hh, ++n) {
         const int h = g * p.G + hh;
         const int s = n & 1;
         if (!(ok = mbar_wait(&bars[kSFull], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
         if (!(ok = mbar_wait(&bars[kDpFull], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
-        if (!(ok = mbar_wait(&bars[kQdoFull + s], (n >> 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        if (!(ok = mbar_wait(&bars[kQFull + s], (n >> 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
         if (n > 0 && !(ok = mbar_wait(&bars[kDsFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
         tc_fence_after();
         const float* lse2 = sLse + s * 128 + qbase;
@@ -365,6 +403,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld16(tl + col, sr);
           tmem_ld16(tl + 128 + col, dr);
           tmem_ld_wait();
+          const uint32_t word = c < 2 ? bw0 : bw1;
           uint32_t pk[8], dk[8];
 #pragma unroll
           for (int e = 0; e < 16; e += 2) {
@@ -372,7 +411,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
               const int qi = c * 16 + e + t;  // 0..63 within this half
-              const uint32_t word = qi < 32 ? bw0 : bw1;
               const bool keep = (word >> (qi & 31)) & 1u;
               float bval = 0.f;
               if (HAS_BIAS) {
@@ -387,63 +425,94 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
             dk[e >> 1] = pack_bf16x2(dv[0], dv[1]);
           }
-          // packed P^T stays inside this warpgroup's own S^T columns (already read), so
-          // queries 0..63 -> cols 0..31 and queries 64..127 -> cols 64..95
+          // packed P^T stays inside this warpgroup's own S^T columns (already read):
+          // queries 0..63 -> cols 0..31, queries 64..127 -> cols 64..95
           tmem_st8(tl + wg * 64 + c * 8, pk);
           // dS^T row j, queries col..col+15: two 16-byte chunks of the SW128 K-major tile
           uint8_t* rowp = sDS + wg * 16384 + j * 128;
-          const int ch0 = c * 2;
-          *reinterpret_cast<uint4*>(rowp + ((ch0 ^ (j & 7)) << 4)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
-          *reinterpret_cast<uint4*>(rowp + (((ch0 + 1) ^ (j & 7)) << 4)) = make_uint4(dk[4], dk[5], dk[6], dk[7]);
+          *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (j & 7)) << 4)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
+          *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (j & 7)) << 4)) = make_uint4(dk[4], dk[5], dk[6], dk[7]);
         }
         fence_proxy_async_smem();
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars[kPReady]);
-        // drain dQ: query row q0 + j, this warpgroup's half of the head dim
+        // drain dQ into the fp32 accumulator
         if (!(ok = mbar_wait(&bars[kDqFull], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
         tc_fence_after();
-        float* dqrow = p.dq_acc + ((static_cast<int64_t>(b) * p.nqpad + q0 + j) * p.Hq + h) * D + wg * (D / 2);
+        if (DQ_T) {
+          // lane = head-dim index j, columns = this warpgroup's 64 queries: each warp
+          // instruction adds 32 consecutive floats of one query row
+          float* dqcol = p.dq_acc + ((static_cast<int64_t>(b) * p.nqpad + q0 + qbase) * p.Hq + h) * D + j;
+          const int64_t rstride = static_cast<int64_t>(p.Hq) * D;
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tl + 128 + wg * (D / 2) + c * 32, r);
-          tmem_ld_wait();
+          for (int c = 0; c < 2; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tl + 128 + qbase + c * 32, r);
+            tmem_ld_wait();
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            red_add_v4(dqrow + c * 32 + 4 * v, __uint_as_float(r[4 * v]) * p.scale,
-                       __uint_as_float(r[4 * v + 1]) * p.scale, __uint_as_float(r[4 * v + 2]) * p.scale,
-                       __uint_as_float(r[4 * v + 3]) * p.scale);
+            for (int t = 0; t < 32; ++t) red_add_f32(dqcol + (c * 32 + t) * rstride, __uint_as_float(r[t]) * p.scale);
+          }
+        } else {
+          float* dqrow = p.dq_acc + ((static_cast<int64_t>(b) * p.nqpad + q0 + j) * p.Hq + h) * D + wg * (D / 2);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tl + 128 + wg * (D / 2) + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              red_add_v4(dqrow + c * 32 + 4 * v, __uint_as_float(r[4 * v]) * p.scale,
+                         __uint_as_float(r[4 * v + 1]) * p.scale, __uint_as_float(r[4 * v + 2]) * p.scale,
+                         __uint_as_float(r[4 * v + 3]) * p.scale);
+          }
         }
         tc_fence_before();
         mbar_arrive(&bars[kDqFree]);
       }
       if (WANT_DBIAS && ok) {
-        uint16_t* dcol = p.dbias + (static_cast<int64_t>(b) * p.Hkv + g) * p.Nq * p.Nk +
-                         static_cast<int64_t>(q0 + qbase) * p.Nk + kidx;
+        // The dS^T tile is free here (the last head's dK / dQ products have completed):
+        // stage this query tile's dBias in it as a (query, key) SW128 tile and TMA-store it.
+        uint8_t* dbt = sDS + (j >> 6) * 16384 + (j & 7) * 2;
+        const int jc = (j & 63) >> 3;
 #pragma unroll
         for (int qi = 0; qi < 64; ++qi) {
-          if (kin && qi < rows_in)
-            dcol[static_cast<int64_t>(qi) * p.Nk] = static_cast<uint16_t>(pack_bf16x2(acc[qi], 0.f) & 0xFFFFu);
+          const int i = qbase + qi;
+          *reinterpret_cast<uint16_t*>(dbt + i * 128 + ((jc ^ (i & 7)) << 4)) =
+              static_cast<uint16_t>(pack_bf16x2(acc[qi], 0.f) & 0xFFFFu);
           acc[qi] = 0.f;
         }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 256);
+        if (ctid == 0) {
+          tma_store_4d(&tmDB, sDS, k0, q0, g, b);
+          tma_store_4d(&tmDB, sDS + 16384, k0 + 64, q0, g, b);
+          bulk_commit_group();
+          bulk_wait_read_all();
+        }
+        named_bar_sync(1, 256);
       }
     }
-    // zero-fill dBias tiles of this key column that were skipped
+    if (ok && n > 0) ok = mbar_wait(&bars[kFinal], 0, p.err, kDevErrTimeout, abort_flag);
+    // zero-fill the dBias tiles of this key column that were skipped (TMA stores of a zero tile)
     if (WANT_DBIAS && ok) {
-      const int cols = min(kTile, p.Nk - k0);
-      const int r = ctid & 127, half = ctid >> 7;
-      for (int qt = 0; qt < p.nTq; ++qt) {
-        if (p.kmap[col_base + static_cast<int64_t>(qt) * p.nTk] != kSkip) continue;
-        const int i = qt * kTile + r;
-        if (i >= p.Nq) continue;
-        uint16_t* drow = p.dbias + ((static_cast<int64_t>(b) * p.Hkv + g) * p.Nq + i) * p.Nk + k0;
-        for (int c = half * 64; c < min(cols, half * 64 + 64); c += 8)
-          *reinterpret_cast<uint4*>(drow + c) = make_uint4(0, 0, 0, 0);
+      reinterpret_cast<uint4*>(sDS)[ctid * 8 + 0] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 1; u < 8; ++u) reinterpret_cast<uint4*>(sDS)[ctid * 8 + u] = make_uint4(0, 0, 0, 0);
+      fence_proxy_async_smem();
+      named_bar_sync(1, 256);
+      if (ctid == 0) {
+        for (int qt = 0; qt < p.nTq; ++qt) {
+          if (p.kmap[col_base + static_cast<int64_t>(qt) * p.nTk] != kSkip) continue;
+          tma_store_4d(&tmDB, sDS, k0, qt * kTile, g, b);
+          tma_store_4d(&tmDB, sDS + 16384, k0 + 64, qt * kTile, g, b);
+        }
+        bulk_commit_group();
+        bulk_wait_all();
       }
+      named_bar_sync(1, 256);
     }
     // dK (warpgroup 0) and dV (warpgroup 1)
-    if (ok && n > 0) ok = mbar_wait(&bars[kFinal], 0, p.err, kDevErrTimeout, abort_flag);
     if (ok) {
       tc_fence_after();
       const int64_t off = ((static_cast<int64_t>(b) * p.Nk + kidx) * p.Hkv + g) * D;
@@ -471,8 +540,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
     }
+   }
   }
-  }
+  if (WANT_DBIAS && threadIdx.x == 128) bulk_wait_all();  // compute thread 0 issued the dBias stores
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -484,18 +554,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 template <int D, bool HB, bool WD>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                         const BwdParams& p, cudaStream_t stream) {
-  using L = BwdSmem<D>;
+                         const CUtensorMap& tb, const CUtensorMap& tdb, const BwdParams& p, cudaStream_t stream) {
+  using L = BwdSmem<D, HB>;
   auto kern = bwd_kernel<D, HB, WD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes fa;
   e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
-  // setmaxnreg re-balancing needs the launch allocation to cover 56 + 2 x 224 per SMSP slot
+  // setmaxnreg re-balancing needs the launch allocation to cover low + 2 x high per SMSP slot
   if (fa.numRegs < kBwdMinLaunchRegs) return cudaErrorInvalidConfiguration;
   const unsigned grid = static_cast<unsigned>(p.nTk) * p.B * p.Hkv;
-  kern<<<grid, kBwdThreads, L::kTotal, stream>>>(tq, tk, tv, tdo, p);
+  kern<<<grid, kBwdThreads, L::kTotal, stream>>>(tq, tk, tv, tdo, tb, tdb, p);
   return cudaGetLastError();
 }
 
@@ -515,16 +585,17 @@ cudaError_t launch_dq_convert(const DqConvertParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_bwd(int d, bool has_bias, bool want_dbias, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tb, const CUtensorMap& tdb,
+                       const BwdParams& p, cudaStream_t stream) {
   if (d == 128) {
-    if (want_dbias) return launch_bwd_t<128, true, true>(tq, tk, tv, tdo, p, stream);
-    return has_bias ? launch_bwd_t<128, true, false>(tq, tk, tv, tdo, p, stream)
-                    : launch_bwd_t<128, false, false>(tq, tk, tv, tdo, p, stream);
+    if (want_dbias) return launch_bwd_t<128, true, true>(tq, tk, tv, tdo, tb, tdb, p, stream);
+    return has_bias ? launch_bwd_t<128, true, false>(tq, tk, tv, tdo, tb, tdb, p, stream)
+                    : launch_bwd_t<128, false, false>(tq, tk, tv, tdo, tb, tdb, p, stream);
   }
   if (d == 64) {
-    if (want_dbias) return launch_bwd_t<64, true, true>(tq, tk, tv, tdo, p, stream);
-    return has_bias ? launch_bwd_t<64, true, false>(tq, tk, tv, tdo, p, stream)
-                    : launch_bwd_t<64, false, false>(tq, tk, tv, tdo, p, stream);
+    if (want_dbias) return launch_bwd_t<64, true, true>(tq, tk, tv, tdo, tb, tdb, p, stream);
+    return has_bias ? launch_bwd_t<64, true, false>(tq, tk, tv, tdo, tb, tdb, p, stream)
+                    : launch_bwd_t<64, false, false>(tq, tk, tv, tdo, tb, tdb, p, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -89,7 +89,8 @@ cudaError_t launch_fwd(int d, bool has_bias, const CUtensorMap& tq, const CUtens
                        const CUtensorMap& tb, const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream);
 cudaError_t launch_bwd(int d, bool has_bias, bool want_dbias, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream);
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tb, const CUtensorMap& tdb,
+                       const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_dq_convert(const DqConvertParams& p, cudaStream_t stream);
 
 }  // namespace fdma
