@@ -33,6 +33,10 @@ WORKLOAD = "n16384_hq16_hkv4"
 METRIC = "effective fwd+bwd TFLOP/s (non-skipped tiles) and % of roofline, 1 GB300"
 TILE = 128
 KERNELS_PER_STEP = 5  # classify, fwd, bwd_pre, bwd, dq_convert
+# DRAM bytes (read + write) of one bwd_kernel launch on this workload, from the ncu capture in
+# profiles/bwd_kernel_n4096.md (714.4 MB on n4096_hq32_hkv8) scaled by active (tile, head) units
+# (x 7.82); None whenever the kernel has changed since that capture.
+BWD_TRAFFIC_BYTES = 5.59e9
 
 
 def _peaks():
@@ -296,7 +300,8 @@ def run_gpu(args):
                      "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                      "peak_source": peaks["source"] + " bf16_tflops_sustained",
                      "frac": round(bwd_achieved / peaks["bf16_tflops_sustained"], 4),
-                     "traffic": None},
+                     "traffic": BWD_TRAFFIC_BYTES,
+                     "traffic_note": "ncu dram bytes of bwd_kernel on N=4096 scaled x7.82 to this workload"},
         "e2e": {"value": round(whole_job_tflops(flops, ws, ms_e2e), 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3)},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
