@@ -36,7 +36,7 @@ KERNELS_PER_STEP = 5  # classify, fwd, bwd_pre, bwd, dq_convert
 # DRAM bytes (read + write) of one bwd_kernel launch on this workload, from the ncu capture in
 # profiles/bwd_kernel_n4096.md (714.4 MB on n4096_hq32_hkv8) scaled by active (tile, head) units
 # (x 7.82); None whenever the kernel has changed since that capture.
-BWD_TRAFFIC_BYTES = 5.59e9
+BWD_TRAFFIC_BYTES = None
 
 
 def _peaks():

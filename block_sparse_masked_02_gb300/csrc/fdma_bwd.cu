@@ -312,6 +312,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         umma_commit(&bars[kDpFull]);
         if (!(ok = mbar_wait(&bars[kPReady], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
         tc_fence_after();
+        // dQ first (K dimension = 128 keys; written over the dP^T columns, which the compute
+        // warps have read): its drain then overlaps the dV / dK products below
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (DQ_T)
+            umma_ss(tbase + 128, kdesc_mn + mnmajor_step(k), dsdesc_mn + mnmajor_step(k), IDESC_DQ, k > 0);
+          else
+            umma_ss(tbase + 128, dsdesc_mn + mnmajor_step(k), kdesc_mn + mnmajor_step(k), IDESC_DQ, k > 0);
+        }
+        umma_commit(&bars[kDqFull]);
         // dV += P^T dO  (K dimension = 128 queries; P^T packed in TMEM cols 0..31 and 64..95)
 #pragma unroll
         for (int k = 0; k < 8; ++k)
@@ -324,15 +334,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           umma_ss(tbase + 384, dsdesc_k + kmajor_step(k, 128), qdesc_mn + mnmajor_step(k), IDESC_DK,
                   (n > 0 || k > 0) ? 1u : 0u);
         umma_commit(&bars[kQEmpty + s]);
-        // dQ (K dimension = 128 keys)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (DQ_T)
-            umma_ss(tbase + 128, kdesc_mn + mnmajor_step(k), dsdesc_mn + mnmajor_step(k), IDESC_DQ, k > 0);
-          else
-            umma_ss(tbase + 128, dsdesc_mn + mnmajor_step(k), kdesc_mn + mnmajor_step(k), IDESC_DQ, k > 0);
-        }
-        umma_commit(&bars[kDqFull]);
         umma_commit(&bars[kDsFree]);
       }
     }
@@ -402,6 +403,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint32_t sr[16], dr[16];
           tmem_ld16(tl + col, sr);
           tmem_ld16(tl + 128 + col, dr);
+          float l16[16], d16[16];  // this chunk's 16 lse / delta values (broadcast 16-byte reads)
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const float4 a = reinterpret_cast<const float4*>(lse2 + c * 16)[v];
+            const float4 bq = reinterpret_cast<const float4*>(dlt + c * 16)[v];
+            l16[4 * v] = a.x; l16[4 * v + 1] = a.y; l16[4 * v + 2] = a.z; l16[4 * v + 3] = a.w;
+            d16[4 * v] = bq.x; d16[4 * v + 1] = bq.y; d16[4 * v + 2] = bq.z; d16[4 * v + 3] = bq.w;
+          }
           tmem_ld_wait();
           const uint32_t word = c < 2 ? bw0 : bw1;
           uint32_t pk[8], dk[8];
@@ -417,9 +426,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const uint32_t w2 = bpk[qi >> 1];
                 bval = __uint_as_float((qi & 1) ? (w2 & 0xFFFF0000u) : (w2 << 16));
               }
-              const float x = fmaf(__uint_as_float(sr[e + t]), p.scale_log2, fmaf(bval, kLog2e, -lse2[qi]));
+              const float x = fmaf(__uint_as_float(sr[e + t]), p.scale_log2, fmaf(bval, kLog2e, -l16[e + t]));
               pv[t] = keep ? ex2(x) : 0.f;
-              dv[t] = pv[t] * (__uint_as_float(dr[e + t]) - dlt[qi]);
+              dv[t] = pv[t] * (__uint_as_float(dr[e + t]) - d16[e + t]);
               if (WANT_DBIAS) acc[qi] += dv[t];
             }
             pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
