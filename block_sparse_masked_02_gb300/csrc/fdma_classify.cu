@@ -35,6 +35,29 @@ __global__ void __launch_bounds__(256) classify_kernel(const ClassifyParams p) {
   }
   const int rows = min(kTile, p.Nq - q0);
   const int cols = min(kTile, p.Nk - k0);
+  const bool ragged = rows < kTile || cols < kTile;
+
+  // Column ranges / no mask away from the causal diagonal: each column masks one
+  // contiguous run of the tile's rows, so the class follows from 128 per-column
+  // counts; only partial (or ragged) tiles need the per-element pass below.
+  if (p.mask_kind != FDMA_MASK_DENSE && !p.no_skip && !(p.causal && k0 + kTile - 1 > q0)) {
+    int masked = 0;
+    if (p.mask_kind == FDMA_MASK_COLRANGES && tid < cols) {
+      const int32_t* src = p.cr + b * p.cr_b + g * p.cr_h + 2 * static_cast<int64_t>(k0 + tid);
+      const int lo = max(src[0], q0), hi = min(src[1], q0 + rows);
+      masked = max(0, hi - lo);
+    }
+    const int all_kept = __syncthreads_and(tid >= cols || masked == 0);
+    const int all_masked = __syncthreads_and(tid >= cols || masked == rows);
+    const int cls = all_masked ? kSkip : (all_kept ? kFull : kPartial);
+    if (cls == kSkip || (cls == kFull && !ragged)) {
+      if (tid == 0) {
+        p.kmap[tile] = static_cast<int8_t>(cls);
+        if (p.user_map) p.user_map[tile] = static_cast<int8_t>(cls);
+      }
+      return;
+    }
+  }
 
   if (p.mask_kind == FDMA_MASK_COLRANGES) {
     if (tid < kTile) {
@@ -103,7 +126,6 @@ __global__ void __launch_bounds__(256) classify_kernel(const ClassifyParams p) {
   any = __syncthreads_or(any);
   all = __syncthreads_and(all);
   const int cls = any ? (all ? kFull : kPartial) : kSkip;
-  const bool ragged = rows < kTile || cols < kTile;
   const int kcls = p.no_skip ? kPartial : cls;
   if (tid == 0) {
     p.kmap[tile] = static_cast<int8_t>(kcls);
