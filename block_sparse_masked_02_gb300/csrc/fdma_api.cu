@@ -67,8 +67,9 @@ int validate(const fdma_args* a, bool need_workspace) {
       break;
     case FDMA_MASK_DENSE:
       if (a->mask == nullptr) return FDMA_ERR_INVALID;
-      if (!aligned16(a->mask) || a->mask_stride[2] % 8 != 0 || a->mask_stride[0] < 0 || a->mask_stride[1] < 0)
-        return FDMA_ERR_UNSUPPORTED;
+      if (!aligned16(a->mask)) return FDMA_ERR_UNSUPPORTED;
+      for (int i = 0; i < 3; ++i)  // rows are read in 16-byte pieces
+        if (a->mask_stride[i] < 0 || a->mask_stride[i] % 8 != 0) return FDMA_ERR_UNSUPPORTED;
       break;
     case FDMA_MASK_COLRANGES:
       if (a->colranges == nullptr) return FDMA_ERR_INVALID;

@@ -2,23 +2,82 @@
 // only when the OR over its mask is true; FlashMask README, "Sparse
 // computation": blocks are fully masked, partially masked or unmasked).
 //
-// One CTA per 128x128 tile.  It reads the tile's dense mask once (16-byte
-// streaming loads), or evaluates the column ranges, ANDs in causality and the
-// bounds, and writes
+// For every 128x128 tile it writes
 //   - the tile class (0 skip / 1 partial / 2 full) for the attention kernels
 //     and, optionally, for the caller;
-//   - for tiles the kernels must mask element-wise (partial, or cut by the
-//     sequence end), two packed keep-bit copies: row-major (forward: one
-//     thread per query row reads 16 bytes) and column-major (backward: one
-//     thread per key reads 16 bytes).
+//   - for tiles the kernels must mask element-wise (partial, or full but cut
+//     by the sequence end), two packed keep-bit copies: row-major (forward:
+//     one thread per query row reads 16 bytes; bit c%32 of word c/32) and
+//     column-major (backward: one thread per key reads 16 bytes; bit r%32 of
+//     word r/32).  Bits outside the sequence are zero.
+//
+// Dense masks: one CTA per tile reads the tile once with 16-byte streaming
+// loads; each thread owns an 8x8 block, so the column-major copy is one 8x8
+// bit transpose per thread.  Column ranges (and no mask): one warp per key tile
+// walks a run of query tiles; skip/full follow from per-column masked-row
+// counts, and keep bits are built a 32-row word at a time from the ranges.
 // Tiles entirely above the causal diagonal are classified without reading.
 #include "fdma_internal.h"
 
 namespace fdma {
 
-__global__ void __launch_bounds__(256) classify_kernel(const ClassifyParams p) {
-  __shared__ uint8_t rowbits[kTile][16];  // bit (c & 7) of byte c >> 3 = keep(q0 + r, k0 + c)
-  __shared__ int2 ranges[kTile];
+namespace {
+
+// Keep bits of 8 bf16 mask values (bit e = value e is nonzero; both signed
+// zeros count as zero).  (x & 0x7FFF) + 0x7FFF has bit 15 set exactly when the
+// magnitude bits are nonzero, with no carry out of the 16-bit half; the two
+// halves' top bytes are then gathered and the eight flags packed by one
+// multiply whose partial products land on distinct bits.
+__device__ __forceinline__ uint32_t keep_byte(const uint4 raw) {
+  const uint32_t y0 = (raw.x & 0x7FFF7FFFu) + 0x7FFF7FFFu;
+  const uint32_t y1 = (raw.y & 0x7FFF7FFFu) + 0x7FFF7FFFu;
+  const uint32_t y2 = (raw.z & 0x7FFF7FFFu) + 0x7FFF7FFFu;
+  const uint32_t y3 = (raw.w & 0x7FFF7FFFu) + 0x7FFF7FFFu;
+  const uint32_t z01 = __byte_perm(y0, y1, 0x7531);  // flags of values 0..3 at bits 7, 15, 23, 31
+  const uint32_t z23 = __byte_perm(y2, y3, 0x7531);  // values 4..7
+  const uint32_t w = ((z01 >> 7) & 0x01010101u) | ((z23 >> 3) & 0x10101010u);
+  return (w * 0x01020408u) >> 24;
+}
+
+// 8x8 bit-matrix transpose (bit 8u+e -> bit 8e+u) by three masked delta swaps
+// (Hacker's Delight, section 7-3, "Transposing a Bit Matrix").
+__device__ __forceinline__ uint64_t transpose8x8(uint64_t x) {
+  uint64_t t = (x ^ (x >> 7)) & 0x00AA00AA00AA00AAull;
+  x ^= t ^ (t << 7);
+  t = (x ^ (x >> 14)) & 0x0000CCCC0000CCCCull;
+  x ^= t ^ (t << 14);
+  t = (x ^ (x >> 28)) & 0x00000000F0F0F0F0ull;
+  x ^= t ^ (t << 28);
+  return x;
+}
+
+// 32x32 bit transpose across a warp: lane l holds row l (bit c = column c) and
+// gets column l.  Five butterfly stages, each swapping the off-diagonal
+// j x j sub-blocks between lanes l and l ^ j (the recursive block transpose of
+// Hacker's Delight, section 7-3, spread over lanes).
+__device__ __forceinline__ uint32_t transpose32_warp(uint32_t x, int lane) {
+#pragma unroll
+  for (int j = 16; j >= 1; j >>= 1) {
+    const uint32_t m = j == 16 ? 0x0000FFFFu : j == 8 ? 0x00FF00FFu : j == 4 ? 0x0F0F0F0Fu : j == 2 ? 0x33333333u
+                                                                                           : 0x55555555u;
+    const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, x, j);
+    x = (lane & j) ? ((x & ~m) | ((y >> j) & m)) : ((x & m) | ((y << j) & ~m));
+  }
+  return x;
+}
+
+__device__ __forceinline__ uint32_t low_bits8(int n) { return n >= 8 ? 0xFFu : (n <= 0 ? 0u : (1u << n) - 1u); }
+__device__ __forceinline__ uint32_t low_bits32(int n) { return n >= 32 ? 0xFFFFFFFFu : (n <= 0 ? 0u : (1u << n) - 1u); }
+
+__device__ __forceinline__ bool needs_bits(int kcls, bool ragged) {
+  return kcls == kPartial || (kcls == kFull && ragged);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(256) classify_dense_kernel(const ClassifyParams p) {
+  __shared__ __align__(16) uint8_t rowbits[kTile][16];  // bit (c & 7) of byte c >> 3 = keep(q0 + r, k0 + c)
+  __shared__ __align__(16) uint8_t colbits[kTile][16];  // bit (r & 7) of byte r >> 3
 
   const int kt = blockIdx.x, qt = blockIdx.y, bg = blockIdx.z;
   const int b = bg / p.Hkv, g = bg % p.Hkv;
@@ -36,118 +95,180 @@ __global__ void __launch_bounds__(256) classify_kernel(const ClassifyParams p) {
   const int rows = min(kTile, p.Nq - q0);
   const int cols = min(kTile, p.Nk - k0);
   const bool ragged = rows < kTile || cols < kTile;
+  const bool diag = p.causal && k0 + kTile - 1 > q0;
 
-  // Column ranges / no mask away from the causal diagonal: each column masks one
-  // contiguous run of the tile's rows, so the class follows from 128 per-column
-  // counts; only partial (or ragged) tiles need the per-element pass below.
-  if (p.mask_kind != FDMA_MASK_DENSE && !p.no_skip && !(p.causal && k0 + kTile - 1 > q0)) {
-    int masked = 0;
-    if (p.mask_kind == FDMA_MASK_COLRANGES && tid < cols) {
-      const int32_t* src = p.cr + b * p.cr_b + g * p.cr_h + 2 * static_cast<int64_t>(k0 + tid);
-      const int lo = max(src[0], q0), hi = min(src[1], q0 + rows);
-      masked = max(0, hi - lo);
-    }
-    const int all_kept = __syncthreads_and(tid >= cols || masked == 0);
-    const int all_masked = __syncthreads_and(tid >= cols || masked == rows);
-    const int cls = all_masked ? kSkip : (all_kept ? kFull : kPartial);
-    if (cls == kSkip || (cls == kFull && !ragged)) {
-      if (tid == 0) {
-        p.kmap[tile] = static_cast<int8_t>(cls);
-        if (p.user_map) p.user_map[tile] = static_cast<int8_t>(cls);
-      }
-      return;
-    }
-  }
-
-  if (p.mask_kind == FDMA_MASK_COLRANGES) {
-    if (tid < kTile) {
-      int2 rg = make_int2(0, 0);
-      if (tid < cols) {
-        const int32_t* src = p.cr + b * p.cr_b + g * p.cr_h + 2 * static_cast<int64_t>(k0 + tid);
-        rg = make_int2(src[0], src[1]);
-      }
-      ranges[tid] = rg;
-    }
-    __syncthreads();
-  }
-
-  // 2048 chunks of 8 columns; thread tid owns chunks tid + 256*u.
-  int any = 0, all = 1;
+  // Thread -> 8x8 block: rows rb*8 .. rb*8+7, columns cc*8 .. cc*8+7.  For each
+  // row step a warp reads two whole 256-byte row segments.
+  const int cc = tid & 15, rb = tid >> 4;
+  const uint16_t* base = p.mask + b * p.ms_b + g * p.ms_h + static_cast<int64_t>(q0 + rb * 8) * p.ms_r + k0 + cc * 8;
+  const int ncol = cols - cc * 8;  // valid columns of this thread's chunk
   uint4 raw[8];
 #pragma unroll
-  for (int u = 0; u < 8; ++u) raw[u] = make_uint4(0, 0, 0, 0);
-  if (p.mask_kind == FDMA_MASK_DENSE) {
+  for (int u = 0; u < 8; ++u) {
+    raw[u] = make_uint4(0, 0, 0, 0);
+    if (rb * 8 + u < rows && ncol > 0) {
+      const uint16_t* src = base + u * p.ms_r;
+      if (ncol >= 8) {
+        raw[u] = __ldcs(reinterpret_cast<const uint4*>(src));
+      } else {
+        uint32_t h[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int e = 0; e < ncol; ++e) h[e] = src[e];
+        raw[u] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+      }
+    }
+  }
+  uint64_t blk = 0;  // bit 8u+e = keep(row rb*8+u, column cc*8+e)
+#pragma unroll
+  for (int u = 0; u < 8; ++u) blk |= static_cast<uint64_t>(keep_byte(raw[u])) << (8 * u);
+
+  uint64_t valid = ~0ull;
+  if (ragged || diag) {
+    const uint32_t cmask = low_bits8(ncol);
+    valid = 0;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int idx = tid + 256 * u, r = idx >> 4, cc = idx & 15;
-      if (r < rows && cc * 8 < cols) {
-        const uint16_t* src = p.mask + b * p.ms_b + g * p.ms_h + static_cast<int64_t>(q0 + r) * p.ms_r + k0 + cc * 8;
-        if (cc * 8 + 8 <= cols) {
-          raw[u] = __ldcs(reinterpret_cast<const uint4*>(src));
-        } else {
-          uint16_t tmp[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-          for (int e = 0; e < cols - cc * 8; ++e) tmp[e] = src[e];
-          raw[u] = make_uint4(tmp[0] | (uint32_t(tmp[1]) << 16), tmp[2] | (uint32_t(tmp[3]) << 16),
-                              tmp[4] | (uint32_t(tmp[5]) << 16), tmp[6] | (uint32_t(tmp[7]) << 16));
-        }
-      }
+      const int r = rb * 8 + u;
+      const uint32_t vm = r < rows ? cmask : 0u;
+      valid |= static_cast<uint64_t>(vm) << (8 * u);
+      // causal: keep only columns j <= i, i.e. c <= r + q0 - k0
+      const uint32_t cm = diag ? low_bits8(r + q0 - k0 - cc * 8 + 1) : 0xFFu;
+      blk &= ~(static_cast<uint64_t>(0xFFu & ~(vm & cm)) << (8 * u));
     }
   }
+
+  // Stage both bit copies; the rotations keep the byte stores of a warp on
+  // distinct banks.
+  const uint64_t tr = transpose8x8(blk);
 #pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const int idx = tid + 256 * u, r = idx >> 4, cc = idx & 15;
-    const int i = q0 + r;
-    uint32_t byte = 0;
-    if (r < rows) {
-      const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int c = cc * 8 + e, j = k0 + c;
-        if (c < cols) {
-          bool keep;
-          if (p.mask_kind == FDMA_MASK_DENSE) {
-            const uint32_t h = (w[e >> 1] >> ((e & 1) * 16)) & 0xFFFFu;
-            keep = (h & 0x7FFFu) != 0;  // nonzero (either sign of zero counts as zero)
-          } else if (p.mask_kind == FDMA_MASK_COLRANGES) {
-            const int2 rg = ranges[c];
-            keep = !(rg.x <= i && i < rg.y);
-          } else {
-            keep = true;
-          }
-          if (p.causal) keep = keep && (j <= i);
-          byte |= static_cast<uint32_t>(keep) << e;
-          any |= keep;
-          all &= keep;
-        }
-      }
-    }
-    rowbits[r][cc] = static_cast<uint8_t>(byte);
+  for (int s = 0; s < 8; ++s) {
+    const int u = (s + 4 * (rb & 1)) & 7;
+    rowbits[rb * 8 + u][cc] = static_cast<uint8_t>(blk >> (8 * u));
+    const int e = (s + cc) & 7;
+    colbits[cc * 8 + e][rb] = static_cast<uint8_t>(tr >> (8 * e));
   }
-  any = __syncthreads_or(any);
-  all = __syncthreads_and(all);
+  const int any = __syncthreads_or(blk != 0);
+  const int all = __syncthreads_and((blk | ~valid) == ~0ull);
   const int cls = any ? (all ? kFull : kPartial) : kSkip;
   const int kcls = p.no_skip ? kPartial : cls;
   if (tid == 0) {
     p.kmap[tile] = static_cast<int8_t>(kcls);
     if (p.user_map) p.user_map[tile] = static_cast<int8_t>(cls);
   }
-  if (kcls == kSkip || (kcls == kFull && !ragged)) return;
+  if (!needs_bits(kcls, ragged)) return;
+  if (tid < kTile)
+    p.bits_row[tile * kTile + tid] = *reinterpret_cast<const uint4*>(rowbits[tid]);
+  else
+    p.bits_col[tile * kTile + tid - kTile] = *reinterpret_cast<const uint4*>(colbits[tid - kTile]);
+}
 
-  if (tid < kTile) p.bits_row[tile * kTile + tid] = *reinterpret_cast<const uint4*>(rowbits[tid]);
-  // column-major: thread -> (column c, half h of the rows)
-  const int c = tid >> 1, h = tid & 1;
-  uint32_t lo = 0, hi = 0;
-#pragma unroll 8
-  for (int rr = 0; rr < 32; ++rr) {
-    lo |= static_cast<uint32_t>((rowbits[h * 64 + rr][c >> 3] >> (c & 7)) & 1u) << rr;
-    hi |= static_cast<uint32_t>((rowbits[h * 64 + 32 + rr][c >> 3] >> (c & 7)) & 1u) << rr;
+// One warp per (batch, kv head, key tile) and run of kRangeChunk query tiles;
+// lane l owns columns l + 32*s.
+constexpr int kRangeChunk = 16;
+
+__global__ void __launch_bounds__(256) classify_ranges_kernel(const ClassifyParams p) {
+  const int lane = threadIdx.x & 31;
+  const int nchunk = (p.nTq + kRangeChunk - 1) / kRangeChunk;
+  const int64_t wid = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (wid >= static_cast<int64_t>(p.B) * p.Hkv * p.nTk * nchunk) return;
+  const int64_t strip = wid / nchunk;
+  const int qt_begin = static_cast<int>(wid % nchunk) * kRangeChunk;
+  const int qt_end = min(p.nTq, qt_begin + kRangeChunk);
+  const int kt = static_cast<int>(strip % p.nTk);
+  const int bg = static_cast<int>(strip / p.nTk);
+  const int b = bg / p.Hkv, g = bg % p.Hkv;
+  const int k0 = kt * kTile, cols = min(kTile, p.Nk - k0);
+
+  // Masked rows of column c are [lo, hi), clamped to [0, Nq] (empty when hi <= lo).
+  int lo[4], hi[4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    lo[s] = hi[s] = 0;
+    const int c = lane + 32 * s;
+    if (p.mask_kind == FDMA_MASK_COLRANGES && c < cols) {
+      const int32_t* src = p.cr + b * p.cr_b + g * p.cr_h + 2 * static_cast<int64_t>(k0 + c);
+      lo[s] = min(max(src[0], 0), p.Nq);
+      hi[s] = min(max(src[1], 0), p.Nq);
+    }
   }
-  reinterpret_cast<uint2*>(&p.bits_col[tile * kTile + c])[h] = make_uint2(lo, hi);
+
+  for (int qt = qt_begin; qt < qt_end; ++qt) {
+    const int q0 = qt * kTile, rows = min(kTile, p.Nq - q0);
+    const int64_t tile = (static_cast<int64_t>(bg) * p.nTq + qt) * p.nTk + kt;
+    const bool ragged = rows < kTile || cols < kTile;
+    const bool above = p.causal && k0 > q0 + kTile - 1;
+    const bool diag = p.causal && k0 + kTile - 1 > q0;  // includes "above"
+    int cls = kSkip;
+    bool exact = false;  // class known without keep bits
+    if (above && !p.no_skip) {
+      exact = true;
+    } else if (!diag && !p.no_skip) {
+      bool kept = true, masked = true;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        if (lane + 32 * s < cols) {
+          const int m = max(0, min(hi[s], q0 + rows) - max(lo[s], q0));
+          kept &= m == 0;
+          masked &= m == rows;
+        }
+      }
+      kept = __all_sync(0xFFFFFFFFu, kept);
+      masked = __all_sync(0xFFFFFFFFu, masked);
+      cls = masked ? kSkip : (kept ? kFull : kPartial);
+      exact = !needs_bits(cls, ragged);
+    }
+    if (!exact) {
+      uint32_t cb[4][4];  // [column slot][row word]: bit r of word w = keep(q0 + 32w + r, column)
+      bool any = false, all = true;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int c = lane + 32 * s;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int r0 = q0 + 32 * w;
+          uint32_t vm = 0, word = 0;
+          if (c < cols) {
+            vm = low_bits32(rows - 32 * w);
+            word = vm & ~(low_bits32(hi[s] - r0) & ~low_bits32(lo[s] - r0));
+            if (p.causal) word &= ~low_bits32(k0 + c - r0);  // keep rows i >= j
+          }
+          any |= word != 0;
+          all &= word == vm;
+          cb[s][w] = word;
+        }
+      }
+      any = __any_sync(0xFFFFFFFFu, any);
+      all = __all_sync(0xFFFFFFFFu, all);
+      cls = any ? (all ? kFull : kPartial) : kSkip;
+      const int kcls = p.no_skip ? kPartial : cls;
+      if (needs_bits(kcls, ragged)) {
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          p.bits_col[tile * kTile + lane + 32 * s] = make_uint4(cb[s][0], cb[s][1], cb[s][2], cb[s][3]);
+        // row-major copy: word s of row 32w + lane = bit lane of every lane's cb[s][w]
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t o[4];
+#pragma unroll
+          for (int s = 0; s < 4; ++s) o[s] = transpose32_warp(cb[s][w], lane);
+          p.bits_row[tile * kTile + 32 * w + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+    if (lane == 0) {
+      p.kmap[tile] = static_cast<int8_t>(p.no_skip ? kPartial : cls);
+      if (p.user_map) p.user_map[tile] = static_cast<int8_t>(cls);
+    }
+  }
 }
 
 cudaError_t launch_classify(const ClassifyParams& p, cudaStream_t stream) {
-  dim3 grid(p.nTk, p.nTq, p.B * p.Hkv);
-  classify_kernel<<<grid, 256, 0, stream>>>(p);
+  if (p.mask_kind == FDMA_MASK_DENSE) {
+    dim3 grid(p.nTk, p.nTq, p.B * p.Hkv);
+    classify_dense_kernel<<<grid, 256, 0, stream>>>(p);
+  } else {
+    const int64_t warps = static_cast<int64_t>(p.B) * p.Hkv * p.nTk * ((p.nTq + kRangeChunk - 1) / kRangeChunk);
+    classify_ranges_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -87,7 +87,8 @@ typedef struct fdma_args {
   /* mask selection (fdma_mask_kind) */
   int32_t mask_kind;
   /* FDMA_MASK_DENSE: bf16 (B,Hkv,Nq,Nk), nonzero = keep; strides (batch, head, row) in elements,
-     columns contiguous; row stride a multiple of 8 elements, base 16-byte aligned. */
+     columns contiguous; every stride a multiple of 8 elements, base 16-byte aligned
+     (else FDMA_ERR_UNSUPPORTED). */
   const void* mask;
   int64_t mask_stride[3];
   /* FDMA_MASK_COLRANGES: int32 (B,Hkv,Nk,2): query rows [start,end) are MASKED for key

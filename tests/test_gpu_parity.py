@@ -143,6 +143,23 @@ def test_colranges_random_ranges_noncausal(F):
     run_and_compare(F, inp, False, 0.09)
 
 
+@pytest.mark.parametrize("flags", [0, 2])
+def test_colranges_ragged_causal(F, flags):
+    """Column ranges on a ragged causal problem (last tile 44 rows), with and
+    without block skipping: exercises keep bits built from ranges on diagonal
+    and ragged tiles."""
+    g = torch.Generator().manual_seed(13)
+    B, N, Hq, Hkv, d = 1, 300, 4, 2, 64
+    s = torch.randint(0, N, (B, Hkv, N), generator=g)
+    ln = torch.randint(0, 160, (B, Hkv, N), generator=g)
+    cr = torch.stack([s, s + ln], -1).to(torch.int32).contiguous()
+    cr[0, 0, 128:256] = torch.tensor([0, N], dtype=torch.int32)  # a key tile masked for every row
+    inp = dict(q=torch.randn(B, N, Hq, d, generator=g).bfloat16(), k=torch.randn(B, N, Hkv, d, generator=g).bfloat16(),
+               v=torch.randn(B, N, Hkv, d, generator=g).bfloat16(),
+               dout=torch.randn(B, N, Hq, d, generator=g).bfloat16(), colranges=cr)
+    run_and_compare(F, inp, True, 0.125, flags=flags)
+
+
 def test_bias_without_dbias(F):
     wl = W.scaled(W.WORKLOADS["tiny_n256_d64"], seed=4)
     run_and_compare(F, W.make_inputs(wl), True, wl.scale, want_dbias=False)
