@@ -449,35 +449,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // drain dQ into the fp32 accumulator
         if (!(ok = mbar_wait(&bars[kDqFull], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
         tc_fence_after();
+        // Both 32-column pieces are read before the columns are released, so the next
+        // step's dP^T product can start while the reductions below are still issuing.
+        // (d = 64: this warpgroup's 32 head-dim columns are one piece)
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tl + 128 + (DQ_T ? qbase : wg * (D / 2)), r0);
+        if (DQ_T) tmem_ld32(tl + 128 + qbase + 32, r1);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[kDqFree]);
         if (DQ_T) {
           // lane = head-dim index j, columns = this warpgroup's 64 queries: each warp
           // instruction adds 32 consecutive floats of one query row
-          float* dqcol = p.dq_acc + ((static_cast<int64_t>(b) * p.nqpad + q0 + qbase) * p.Hq + h) * D + j;
           const int64_t rstride = static_cast<int64_t>(p.Hq) * D;
+          float* dst = p.dq_acc + ((static_cast<int64_t>(b) * p.nqpad + q0 + qbase) * p.Hq + h) * D + j;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tl + 128 + qbase + c * 32, r);
-            tmem_ld_wait();
+          for (int t = 0; t < 32; ++t, dst += rstride) red_add_f32(dst, __uint_as_float(r0[t]) * p.scale);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) red_add_f32(dqcol + (c * 32 + t) * rstride, __uint_as_float(r[t]) * p.scale);
-          }
+          for (int t = 0; t < 32; ++t, dst += rstride) red_add_f32(dst, __uint_as_float(r1[t]) * p.scale);
         } else {
           float* dqrow = p.dq_acc + ((static_cast<int64_t>(b) * p.nqpad + q0 + j) * p.Hq + h) * D + wg * (D / 2);
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tl + 128 + wg * (D / 2) + c * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              red_add_v4(dqrow + c * 32 + 4 * v, __uint_as_float(r[4 * v]) * p.scale,
-                         __uint_as_float(r[4 * v + 1]) * p.scale, __uint_as_float(r[4 * v + 2]) * p.scale,
-                         __uint_as_float(r[4 * v + 3]) * p.scale);
-          }
+          for (int v = 0; v < 8; ++v)
+            red_add_v4(dqrow + 4 * v, __uint_as_float(r0[4 * v]) * p.scale, __uint_as_float(r0[4 * v + 1]) * p.scale,
+                       __uint_as_float(r0[4 * v + 2]) * p.scale, __uint_as_float(r0[4 * v + 3]) * p.scale);
         }
-        tc_fence_before();
-        mbar_arrive(&bars[kDqFree]);
       }
       if (WANT_DBIAS && ok) {
         // The dS^T tile is free here (the last head's dK / dQ products have completed):
