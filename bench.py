@@ -33,10 +33,10 @@ WORKLOAD = "n16384_hq16_hkv4"
 METRIC = "effective fwd+bwd TFLOP/s (non-skipped tiles) and % of roofline, 1 GB300"
 TILE = 128
 KERNELS_PER_STEP = 5  # classify, fwd, bwd_pre, bwd, dq_convert
-# DRAM bytes (read + write) of one bwd_kernel launch on this workload, from the ncu capture in
-# profiles/bwd_kernel_n4096.md (714.4 MB on n4096_hq32_hkv8) scaled by active (tile, head) units
-# (x 7.82); None whenever the kernel has changed since that capture.
-BWD_TRAFFIC_BYTES = None
+# DRAM bytes (read + write) of one bwd_kernel launch on this workload: an ncu capture of
+# bwd_kernel on n4096_hq32_hkv8 (360.30 MB read + 353.32 MB written) scaled by the active
+# (tile, head) units, 132096 / 16896; None whenever the kernel has changed since that capture.
+BWD_TRAFFIC_BYTES = round((360.300032e6 + 353.323264e6) * 132096 / 16896)
 
 
 def _peaks():
