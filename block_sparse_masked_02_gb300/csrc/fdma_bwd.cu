@@ -361,7 +361,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int c = 0; c < (WANT_DBIAS ? 64 : 1); ++c) acc[c] = 0.f;
     int n = 0, qi_count = 0;
     bool ok = true;
-    for (int qt = first_qt; ok && qt < p.nTq; qt = it.next(qt), ++qi_count) {
+    // No compute thread leaves these loops early, so every one of them reaches every named
+    // barrier below; after a failed wait (ok == false) the work and the stores are skipped.
+    for (int qt = first_qt; qt < p.nTq; qt = it.next(qt), ++qi_count) {
       const int q0 = qt * kTile;
       const int64_t tile = col_base + static_cast<int64_t>(qt) * p.nTk;
       const bool partial = p.kmap[tile] == kPartial || ragged_k || (ragged_q_any && qt == p.nTq - 1);
@@ -375,7 +377,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // bias^T column slice of this query tile, copied once into registers for every head
       uint32_t bpk[HAS_BIAS ? 32 : 1];
       if (HAS_BIAS) {
-        if (!(ok = mbar_wait(&bars[kBFull], qi_count & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        ok = ok && mbar_wait(&bars[kBFull], qi_count & 1, p.err, kDevErrTimeout, abort_flag);
         const uint8_t* bt = sBias + (j >> 6) * 16384 + (j & 7) * 2;
         const int jc = (j & 63) >> 3;
 #pragma unroll
@@ -390,10 +392,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int hh = 0; hh < p.G; ++hh, ++n) {
         const int h = g * p.G + hh;
         const int s = n & 1;
-        if (!(ok = mbar_wait(&bars[kSFull], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
-        if (!(ok = mbar_wait(&bars[kDpFull], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
-        if (!(ok = mbar_wait(&bars[kQFull + s], (n >> 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
-        if (n > 0 && !(ok = mbar_wait(&bars[kDsFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        ok = ok && mbar_wait(&bars[kSFull], n & 1, p.err, kDevErrTimeout, abort_flag);
+        ok = ok && mbar_wait(&bars[kDpFull], n & 1, p.err, kDevErrTimeout, abort_flag);
+        ok = ok && mbar_wait(&bars[kQFull + s], (n >> 1) & 1, p.err, kDevErrTimeout, abort_flag);
+        ok = ok && (n == 0 || mbar_wait(&bars[kDsFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag));
+        if (!ok) continue;
         tc_fence_after();
         const float* lse2 = sLse + s * 128 + qbase;
         const float* dlt = sDelta + s * 128 + qbase;
@@ -447,7 +450,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_before();
         mbar_arrive(&bars[kPReady]);
         // drain dQ into the fp32 accumulator
-        if (!(ok = mbar_wait(&bars[kDqFull], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        if (!(ok = mbar_wait(&bars[kDqFull], n & 1, p.err, kDevErrTimeout, abort_flag))) continue;
         tc_fence_after();
         // Both 32-column pieces are read before the columns are released, so the next
         // step's dP^T product can start while the reductions below are still issuing.
@@ -475,21 +478,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        __uint_as_float(r0[4 * v + 2]) * p.scale, __uint_as_float(r0[4 * v + 3]) * p.scale);
         }
       }
-      if (WANT_DBIAS && ok) {
-        // The dS^T tile is free here (the last head's dK / dQ products have completed):
-        // stage this query tile's dBias in it as a (query, key) SW128 tile and TMA-store it.
+      if (WANT_DBIAS) {
+        // Once the last head's dQ / dK products are done with the dS^T tile, stage this
+        // query tile's dBias in it as a (query, key) SW128 tile and TMA-store it.
+        ok = ok && mbar_wait(&bars[kDsFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag);
         uint8_t* dbt = sDS + (j >> 6) * 16384 + (j & 7) * 2;
         const int jc = (j & 63) >> 3;
 #pragma unroll
         for (int qi = 0; qi < 64; ++qi) {
           const int i = qbase + qi;
-          *reinterpret_cast<uint16_t*>(dbt + i * 128 + ((jc ^ (i & 7)) << 4)) =
-              static_cast<uint16_t>(pack_bf16x2(acc[qi], 0.f) & 0xFFFFu);
+          if (ok)
+            *reinterpret_cast<uint16_t*>(dbt + i * 128 + ((jc ^ (i & 7)) << 4)) =
+                static_cast<uint16_t>(pack_bf16x2(acc[qi], 0.f) & 0xFFFFu);
           acc[qi] = 0.f;
         }
         fence_proxy_async_smem();
         named_bar_sync(1, 256);
-        if (ctid == 0) {
+        if (ctid == 0 && ok) {
           tma_store_4d(&tmDB, sDS, k0, q0, g, b);
           tma_store_4d(&tmDB, sDS + 16384, k0 + 64, q0, g, b);
           bulk_commit_group();
@@ -500,13 +505,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (ok && n > 0) ok = mbar_wait(&bars[kFinal], 0, p.err, kDevErrTimeout, abort_flag);
     // zero-fill the dBias tiles of this key column that were skipped (TMA stores of a zero tile)
-    if (WANT_DBIAS && ok) {
+    if (WANT_DBIAS) {
       reinterpret_cast<uint4*>(sDS)[ctid * 8 + 0] = make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int u = 1; u < 8; ++u) reinterpret_cast<uint4*>(sDS)[ctid * 8 + u] = make_uint4(0, 0, 0, 0);
       fence_proxy_async_smem();
       named_bar_sync(1, 256);
-      if (ctid == 0) {
+      if (ctid == 0 && ok) {
         for (int qt = 0; qt < p.nTq; ++qt) {
           if (p.kmap[col_base + static_cast<int64_t>(qt) * p.nTk] != kSkip) continue;
           tma_store_4d(&tmDB, sDS, k0, qt * kTile, g, b);
