@@ -232,6 +232,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmDO);
     if (HAS_BIAS) tma_prefetch_desc(&tmB);
+    const uint64_t bias_pol = l2_evict_first();  // each bias tile is read once here
     mbar_arrive_expect_tx(&bars[kKVFull], 2 * L::kQB);
 #pragma unroll
     for (int c = 0; c < KB; ++c) {
@@ -245,7 +246,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!(ok = mbar_wait(&bars[kBEmpty], (qi_count & 1) ^ 1, p.err, kDevErrTimeout, abort_flag))) break;
         mbar_arrive_expect_tx(&bars[kBFull], 32768);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) tma_load_4d(sBias + c * 16384, &tmB, &bars[kBFull], k0 + c * 64, qt * kTile, g, b);
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d_hint(sBias + c * 16384, &tmB, &bars[kBFull], k0 + c * 64, qt * kTile, g, b, bias_pol);
       }
       for (int hh = 0; hh < p.G; ++hh, ++n) {
         const int h = g * p.G + hh;
@@ -495,8 +497,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         fence_proxy_async_smem();
         named_bar_sync(1, 256);
         if (ctid == 0 && ok) {
-          tma_store_4d(&tmDB, sDS, k0, q0, g, b);
-          tma_store_4d(&tmDB, sDS + 16384, k0 + 64, q0, g, b);
+          const uint64_t pol = l2_evict_first();  // dBias is written once, never read here
+          tma_store_4d_hint(&tmDB, sDS, k0, q0, g, b, pol);
+          tma_store_4d_hint(&tmDB, sDS + 16384, k0 + 64, q0, g, b, pol);
           bulk_commit_group();
           bulk_wait_read_all();
         }
@@ -512,10 +515,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       fence_proxy_async_smem();
       named_bar_sync(1, 256);
       if (ctid == 0 && ok) {
+        const uint64_t zpol = l2_evict_first();
         for (int qt = 0; qt < p.nTq; ++qt) {
           if (p.kmap[col_base + static_cast<int64_t>(qt) * p.nTk] != kSkip) continue;
-          tma_store_4d(&tmDB, sDS, k0, qt * kTile, g, b);
-          tma_store_4d(&tmDB, sDS + 16384, k0 + 64, qt * kTile, g, b);
+          tma_store_4d_hint(&tmDB, sDS, k0, qt * kTile, g, b, zpol);
+          tma_store_4d_hint(&tmDB, sDS + 16384, k0 + 64, qt * kTile, g, b, zpol);
         }
         bulk_commit_group();
         bulk_wait_all();

@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(192, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       if (HAS_BIAS) tma_prefetch_desc(&tmB);
+      const uint64_t bias_pol = l2_evict_first();  // each bias tile is read once
       mbar_arrive_expect_tx(&bars[kQFull], L::kQB);
 #pragma unroll
       for (int c = 0; c < KB; ++c) tma_load_4d(sQ + c * 16384, &tmQ, &bars[kQFull], c * 64, q0, h, b);
@@ -163,7 +164,7 @@ __global__ void __launch_bounds__(192, 1)
           mbar_arrive_expect_tx(&bars[kBFull + s], L::kBB);
 #pragma unroll
           for (int c = 0; c < 2; ++c)
-            tma_load_4d(sB + s * L::kBB + c * 16384, &tmB, &bars[kBFull + s], k0 + c * 64, q0, g, b);
+            tma_load_4d_hint(sB + s * L::kBB + c * 16384, &tmB, &bars[kBFull + s], k0 + c * 64, q0, g, b, bias_pol);
         }
         if (!mbar_wait(&bars[kVEmpty + s], ph, p.err, kDevErrTimeout, abort_flag)) break;
         mbar_arrive_expect_tx(&bars[kVFull + s], L::kQB);
@@ -492,6 +493,7 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       if (HAS_BIAS) tma_prefetch_desc(&tmB);
+      const uint64_t bias_pol = l2_evict_first();  // each bias tile is read once
       mbar_arrive_expect_tx(&bars[k2QFull], 2 * L::kQB);
 #pragma unroll
       for (int w = 0; w < 2; ++w)
@@ -518,7 +520,7 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
           mbar_arrive_expect_tx(&bars[k2BFull + sb], L::kBB);
 #pragma unroll
           for (int c = 0; c < 2; ++c)
-            tma_load_4d(sB + sb * L::kBB + c * 16384, &tmB, &bars[k2BFull + sb], k0 + c * 64, q0, g, b);
+            tma_load_4d_hint(sB + sb * L::kBB + c * 16384, &tmB, &bars[k2BFull + sb], k0 + c * 64, q0, g, b, bias_pol);
         }
         // V_n
         {
