@@ -55,7 +55,6 @@ int validate(const fdma_args* a, bool need_workspace) {
   if (a->d != 64 && a->d != 128) return FDMA_ERR_UNSUPPORTED;
   if (cdiv(a->Nk, kTile) > kMaxKTiles || cdiv(a->Nq, kTile) > kMaxKTiles) return FDMA_ERR_UNSUPPORTED;
   if (!(std::isfinite(a->scale) && a->scale > 0.f)) return FDMA_ERR_INVALID;
-  if (a->is_causal && a->Nq != a->Nk) return FDMA_ERR_UNSUPPORTED;
   if (a->q == nullptr || a->k == nullptr || a->v == nullptr) return FDMA_ERR_INVALID;
   for (const void* p : {a->q, a->k, a->v})
     if (!aligned16(p)) return FDMA_ERR_UNSUPPORTED;
@@ -66,12 +65,14 @@ int validate(const fdma_args* a, bool need_workspace) {
     case FDMA_MASK_NONE:
       break;
     case FDMA_MASK_DENSE:
+    case FDMA_MASK_DENSE_U8:
       if (a->mask == nullptr) return FDMA_ERR_INVALID;
       if (!aligned16(a->mask)) return FDMA_ERR_UNSUPPORTED;
-      for (int i = 0; i < 3; ++i)  // rows are read in 16-byte pieces
+      for (int i = 0; i < 3; ++i)  // rows are read in pieces of 8 elements
         if (a->mask_stride[i] < 0 || a->mask_stride[i] % 8 != 0) return FDMA_ERR_UNSUPPORTED;
       break;
     case FDMA_MASK_COLRANGES:
+    case FDMA_MASK_COLRANGES2:
       if (a->colranges == nullptr) return FDMA_ERR_INVALID;
       if (a->cr_stride[0] < 0 || a->cr_stride[1] < 0) return FDMA_ERR_INVALID;
       break;
@@ -83,6 +84,7 @@ int validate(const fdma_args* a, bool need_workspace) {
     if (a->Nk % 8 != 0) return FDMA_ERR_UNSUPPORTED;
     for (int i = 0; i < 3; ++i)
       if (a->bias_stride[i] < 0 || (a->bias_stride[i] * 2) % 16 != 0) return FDMA_ERR_UNSUPPORTED;
+    if (a->bias_stride[2] == 0 && a->Nq > 1) return FDMA_ERR_UNSUPPORTED;  // rows must be distinct
   }
   if (need_workspace && (a->workspace == nullptr || (reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0))
     return FDMA_ERR_WORKSPACE;
@@ -98,7 +100,8 @@ bool make_map(CUtensorMap* m, const void* base, const uint64_t dims[4], const ui
   cuuint64_t gs[3];
   for (int i = 0; i < 3; ++i) {
     uint64_t s = strides_b[i];
-    if (s == 0 || dims[i + 1] == 1) s = (s == 0) ? 16 : s;  // unused extent-1 dims
+    // an extent-1 (unused or broadcast) dim given stride 0 gets the stride of a packed layout
+    if (s == 0) s = (i == 0) ? ((dims[0] * 2 + 15) / 16) * 16 : gs[i - 1] * dims[i];
     gs[i] = s;
   }
   cuuint32_t box[4] = {64, 128, 1, 1};
@@ -106,6 +109,17 @@ bool make_map(CUtensorMap* m, const void* base, const uint64_t dims[4], const ui
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), gd, gs, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Bias (B,Hkv,Nq,Nk) as a 4D map; an axis with stride 0 (broadcast) gets extent 1 and is
+// addressed with coordinate 0 by the kernels (bias_bsel / bias_hsel = 0).
+bool bias_map(CUtensorMap* m, const fdma_args* a) {
+  const bool bb = a->bias_stride[0] == 0, bh = a->bias_stride[1] == 0;
+  const uint64_t dims[4] = {static_cast<uint64_t>(a->Nk), static_cast<uint64_t>(a->Nq),
+                            bh ? 1ull : static_cast<uint64_t>(a->Hkv), bb ? 1ull : static_cast<uint64_t>(a->B)};
+  const uint64_t sb[3] = {static_cast<uint64_t>(a->bias_stride[2]) * 2, static_cast<uint64_t>(a->bias_stride[1]) * 2,
+                          static_cast<uint64_t>(a->bias_stride[0]) * 2};
+  return make_map(m, a->bias, dims, sb);
 }
 
 bool bshd_map(CUtensorMap* m, const void* base, int B, int N, int H, int d, const int64_t st[3]) {
@@ -129,8 +143,10 @@ int classify_into_workspace(const fdma_args* a, int8_t* user_map, cudaStream_t s
   p.nTk = cdiv(a->Nk, kTile);
   p.mask_kind = a->mask_kind;
   p.causal = a->is_causal ? 1 : 0;
+  p.causal_off = a->Nk - a->Nq;
   p.no_skip = (a->flags & FDMA_FLAG_NO_SKIP) ? 1 : 0;
   p.mask = static_cast<const uint16_t*>(a->mask);
+  p.mask_u8 = static_cast<const uint8_t*>(a->mask);
   p.ms_b = a->mask_stride[0];
   p.ms_h = a->mask_stride[1];
   p.ms_r = a->mask_stride[2];
@@ -213,13 +229,7 @@ int fdma_fwd(const fdma_args* a, void* out, float* lse, void* stream_v) {
     return FDMA_ERR_UNSUPPORTED;
   const bool has_bias = a->bias != nullptr;
   if (has_bias) {
-    const uint64_t dims[4] = {static_cast<uint64_t>(a->Nk), static_cast<uint64_t>(a->Nq),
-                              static_cast<uint64_t>(a->Hkv), static_cast<uint64_t>(a->B)};
-    const uint64_t sb[3] = {static_cast<uint64_t>(a->bias_stride[2]) * 2, static_cast<uint64_t>(a->bias_stride[1]) * 2,
-                            static_cast<uint64_t>(a->bias_stride[0]) * 2};
-    if ((a->B > 1 && a->bias_stride[0] == 0) || (a->Hkv > 1 && a->bias_stride[1] == 0) || a->bias_stride[2] == 0)
-      return FDMA_ERR_UNSUPPORTED;
-    if (!make_map(&tb, a->bias, dims, sb)) return FDMA_ERR_UNSUPPORTED;
+    if (!bias_map(&tb, a)) return FDMA_ERR_UNSUPPORTED;
   } else {
     tb = tq;
   }
@@ -233,6 +243,8 @@ int fdma_fwd(const fdma_args* a, void* out, float* lse, void* stream_v) {
   p.nTq = cdiv(a->Nq, kTile);
   p.nTk = cdiv(a->Nk, kTile);
   p.scale_log2 = a->scale * 1.4426950408889634f;
+  p.bias_bsel = a->bias_stride[0] == 0 ? 0 : 1;
+  p.bias_hsel = a->bias_stride[1] == 0 ? 0 : 1;
   p.kmap = reinterpret_cast<const int8_t*>(ws + w.kmap);
   p.bits_row = reinterpret_cast<const uint4*>(ws + w.bits_row);
   p.out = static_cast<uint16_t*>(out);
@@ -304,6 +316,8 @@ int fdma_bwd(const fdma_args* a, const void* out, const void* dout, const float*
   p.bs_b = a->bias_stride[0];
   p.bs_h = a->bias_stride[1];
   p.bs_r = a->bias_stride[2];
+  p.bias_bsel = a->bias_stride[0] == 0 ? 0 : 1;
+  p.bias_hsel = a->bias_stride[1] == 0 ? 0 : 1;
   p.lse2 = pp.lse2;
   p.delta = pp.delta;
   p.dq_acc = pp.dq_acc;
@@ -313,13 +327,7 @@ int fdma_bwd(const fdma_args* a, const void* out, const void* dout, const float*
   p.err = err;
   CUtensorMap tb = tq;
   if (a->bias != nullptr) {
-    const uint64_t dims[4] = {static_cast<uint64_t>(a->Nk), static_cast<uint64_t>(a->Nq),
-                              static_cast<uint64_t>(a->Hkv), static_cast<uint64_t>(a->B)};
-    const uint64_t sb[3] = {static_cast<uint64_t>(a->bias_stride[2]) * 2, static_cast<uint64_t>(a->bias_stride[1]) * 2,
-                            static_cast<uint64_t>(a->bias_stride[0]) * 2};
-    if ((a->B > 1 && a->bias_stride[0] == 0) || (a->Hkv > 1 && a->bias_stride[1] == 0) || a->bias_stride[2] == 0)
-      return FDMA_ERR_UNSUPPORTED;
-    if (!make_map(&tb, a->bias, dims, sb)) return FDMA_ERR_UNSUPPORTED;
+    if (!bias_map(&tb, a)) return FDMA_ERR_UNSUPPORTED;
   }
   CUtensorMap tdb = tq;
   if (dbias != nullptr) {

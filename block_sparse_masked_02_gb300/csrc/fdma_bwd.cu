@@ -247,7 +247,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive_expect_tx(&bars[kBFull], 32768);
 #pragma unroll
         for (int c = 0; c < 2; ++c)
-          tma_load_4d_hint(sBias + c * 16384, &tmB, &bars[kBFull], k0 + c * 64, qt * kTile, g, b, bias_pol);
+          tma_load_4d_hint(sBias + c * 16384, &tmB, &bars[kBFull], k0 + c * 64, qt * kTile, g * p.bias_hsel,
+                           b * p.bias_bsel, bias_pol);
       }
       for (int hh = 0; hh < p.G; ++hh, ++n) {
         const int h = g * p.G + hh;

@@ -17,6 +17,8 @@
 // walks a run of query tiles; skip/full follow from per-column masked-row
 // counts, and keep bits are built a 32-row word at a time from the ranges.
 // Tiles entirely above the causal diagonal are classified without reading.
+// Causality is bottom-right aligned: key j is visible from query i when
+// j <= i + (Nk - Nq), i.e. the usual j <= i for square problems.
 #include "fdma_internal.h"
 
 namespace fdma {
@@ -36,6 +38,16 @@ __device__ __forceinline__ uint32_t keep_byte(const uint4 raw) {
   const uint32_t z01 = __byte_perm(y0, y1, 0x7531);  // flags of values 0..3 at bits 7, 15, 23, 31
   const uint32_t z23 = __byte_perm(y2, y3, 0x7531);  // values 4..7
   const uint32_t w = ((z01 >> 7) & 0x01010101u) | ((z23 >> 3) & 0x10101010u);
+  return (w * 0x01020408u) >> 24;
+}
+
+// Keep bits of 8 uint8 mask values: bit 7 of (x & 0x7F) + 0x7F, or-ed with x, is set
+// exactly when the byte is nonzero; the four top bits of each word are gathered
+// the same way as for bf16.
+__device__ __forceinline__ uint32_t keep_byte_u8(const uint2 raw) {
+  const uint32_t y0 = ((raw.x & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | raw.x;  // flags of values 0..3 at bits 7, 15, 23, 31
+  const uint32_t y1 = ((raw.y & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | raw.y;  // values 4..7
+  const uint32_t w = ((y0 >> 7) & 0x01010101u) | ((y1 >> 3) & 0x10101010u);
   return (w * 0x01020408u) >> 24;
 }
 
@@ -75,6 +87,7 @@ __device__ __forceinline__ bool needs_bits(int kcls, bool ragged) {
 
 }  // namespace
 
+template <bool U8>
 __global__ void __launch_bounds__(256) classify_dense_kernel(const ClassifyParams p) {
   __shared__ __align__(16) uint8_t rowbits[kTile][16];  // bit (c & 7) of byte c >> 3 = keep(q0 + r, k0 + c)
   __shared__ __align__(16) uint8_t colbits[kTile][16];  // bit (r & 7) of byte r >> 3
@@ -85,7 +98,7 @@ __global__ void __launch_bounds__(256) classify_dense_kernel(const ClassifyParam
   const int q0 = qt * kTile, k0 = kt * kTile;
   const int tid = threadIdx.x;
 
-  if (p.causal && k0 > q0 + kTile - 1 && !p.no_skip) {
+  if (p.causal && k0 > q0 + kTile - 1 + p.causal_off && !p.no_skip) {
     if (tid == 0) {
       p.kmap[tile] = kSkip;
       if (p.user_map) p.user_map[tile] = kSkip;
@@ -95,31 +108,54 @@ __global__ void __launch_bounds__(256) classify_dense_kernel(const ClassifyParam
   const int rows = min(kTile, p.Nq - q0);
   const int cols = min(kTile, p.Nk - k0);
   const bool ragged = rows < kTile || cols < kTile;
-  const bool diag = p.causal && k0 + kTile - 1 > q0;
+  const bool diag = p.causal && k0 + kTile - 1 > q0 + p.causal_off;
 
   // Thread -> 8x8 block: rows rb*8 .. rb*8+7, columns cc*8 .. cc*8+7.  For each
   // row step a warp reads two whole 256-byte row segments.
   const int cc = tid & 15, rb = tid >> 4;
-  const uint16_t* base = p.mask + b * p.ms_b + g * p.ms_h + static_cast<int64_t>(q0 + rb * 8) * p.ms_r + k0 + cc * 8;
+  const int64_t off = b * p.ms_b + g * p.ms_h + static_cast<int64_t>(q0 + rb * 8) * p.ms_r + k0 + cc * 8;
   const int ncol = cols - cc * 8;  // valid columns of this thread's chunk
-  uint4 raw[8];
+  uint64_t blk = 0;                // bit 8u+e = keep(row rb*8+u, column cc*8+e)
+  if (U8) {
+    const uint8_t* base = p.mask_u8 + off;
+    uint2 raw[8];
 #pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    raw[u] = make_uint4(0, 0, 0, 0);
-    if (rb * 8 + u < rows && ncol > 0) {
-      const uint16_t* src = base + u * p.ms_r;
-      if (ncol >= 8) {
-        raw[u] = __ldcs(reinterpret_cast<const uint4*>(src));
-      } else {
-        uint32_t h[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int e = 0; e < ncol; ++e) h[e] = src[e];
-        raw[u] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+    for (int u = 0; u < 8; ++u) {
+      raw[u] = make_uint2(0, 0);
+      if (rb * 8 + u < rows && ncol > 0) {
+        const uint8_t* src = base + u * p.ms_r;
+        if (ncol >= 8) {
+          raw[u] = __ldcs(reinterpret_cast<const uint2*>(src));
+        } else {
+          uint32_t h[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+          for (int e = 0; e < ncol; ++e) h[e] = src[e];
+          raw[u] = make_uint2(h[0] | (h[1] << 8) | (h[2] << 16) | (h[3] << 24),
+                              h[4] | (h[5] << 8) | (h[6] << 16) | (h[7] << 24));
+        }
       }
     }
-  }
-  uint64_t blk = 0;  // bit 8u+e = keep(row rb*8+u, column cc*8+e)
 #pragma unroll
-  for (int u = 0; u < 8; ++u) blk |= static_cast<uint64_t>(keep_byte(raw[u])) << (8 * u);
+    for (int u = 0; u < 8; ++u) blk |= static_cast<uint64_t>(keep_byte_u8(raw[u])) << (8 * u);
+  } else {
+    const uint16_t* base = p.mask + off;
+    uint4 raw[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      raw[u] = make_uint4(0, 0, 0, 0);
+      if (rb * 8 + u < rows && ncol > 0) {
+        const uint16_t* src = base + u * p.ms_r;
+        if (ncol >= 8) {
+          raw[u] = __ldcs(reinterpret_cast<const uint4*>(src));
+        } else {
+          uint32_t h[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+          for (int e = 0; e < ncol; ++e) h[e] = src[e];
+          raw[u] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) blk |= static_cast<uint64_t>(keep_byte(raw[u])) << (8 * u);
+  }
 
   uint64_t valid = ~0ull;
   if (ragged || diag) {
@@ -130,8 +166,8 @@ __global__ void __launch_bounds__(256) classify_dense_kernel(const ClassifyParam
       const int r = rb * 8 + u;
       const uint32_t vm = r < rows ? cmask : 0u;
       valid |= static_cast<uint64_t>(vm) << (8 * u);
-      // causal: keep only columns j <= i, i.e. c <= r + q0 - k0
-      const uint32_t cm = diag ? low_bits8(r + q0 - k0 - cc * 8 + 1) : 0xFFu;
+      // causal: keep only columns j <= i + off, i.e. c <= r + q0 + off - k0
+      const uint32_t cm = diag ? low_bits8(r + q0 + p.causal_off - k0 - cc * 8 + 1) : 0xFFu;
       blk &= ~(static_cast<uint64_t>(0xFFu & ~(vm & cm)) << (8 * u));
     }
   }
@@ -178,16 +214,23 @@ __global__ void __launch_bounds__(256) classify_ranges_kernel(const ClassifyPara
   const int b = bg / p.Hkv, g = bg % p.Hkv;
   const int k0 = kt * kTile, cols = min(kTile, p.Nk - k0);
 
-  // Masked rows of column c are [lo, hi), clamped to [0, Nq] (empty when hi <= lo).
-  int lo[4], hi[4];
+  // Masked rows of column c are [lo, hi) and (second kind) [lo2, hi2), clamped to
+  // [0, Nq] (a range is empty when hi <= lo).
+  const bool two = p.mask_kind == FDMA_MASK_COLRANGES2;
+  const int per = two ? 4 : 2;
+  int lo[4], hi[4], lo2[4], hi2[4];
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
-    lo[s] = hi[s] = 0;
+    lo[s] = hi[s] = lo2[s] = hi2[s] = 0;
     const int c = lane + 32 * s;
-    if (p.mask_kind == FDMA_MASK_COLRANGES && c < cols) {
-      const int32_t* src = p.cr + b * p.cr_b + g * p.cr_h + 2 * static_cast<int64_t>(k0 + c);
+    if (p.mask_kind != FDMA_MASK_NONE && c < cols) {
+      const int32_t* src = p.cr + b * p.cr_b + g * p.cr_h + per * static_cast<int64_t>(k0 + c);
       lo[s] = min(max(src[0], 0), p.Nq);
       hi[s] = min(max(src[1], 0), p.Nq);
+      if (two) {
+        lo2[s] = min(max(src[2], 0), p.Nq);
+        hi2[s] = min(max(src[3], 0), p.Nq);
+      }
     }
   }
 
@@ -195,8 +238,8 @@ __global__ void __launch_bounds__(256) classify_ranges_kernel(const ClassifyPara
     const int q0 = qt * kTile, rows = min(kTile, p.Nq - q0);
     const int64_t tile = (static_cast<int64_t>(bg) * p.nTq + qt) * p.nTk + kt;
     const bool ragged = rows < kTile || cols < kTile;
-    const bool above = p.causal && k0 > q0 + kTile - 1;
-    const bool diag = p.causal && k0 + kTile - 1 > q0;  // includes "above"
+    const bool above = p.causal && k0 > q0 + kTile - 1 + p.causal_off;
+    const bool diag = p.causal && k0 + kTile - 1 > q0 + p.causal_off;  // includes "above"
     int cls = kSkip;
     bool exact = false;  // class known without keep bits
     if (above && !p.no_skip) {
@@ -206,7 +249,13 @@ __global__ void __launch_bounds__(256) classify_ranges_kernel(const ClassifyPara
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         if (lane + 32 * s < cols) {
-          const int m = max(0, min(hi[s], q0 + rows) - max(lo[s], q0));
+          // masked rows of the tile: |R1 ∩ T| + |R2 ∩ T| - |R1 ∩ R2 ∩ T|
+          const int q1 = q0 + rows;
+          int m = max(0, min(hi[s], q1) - max(lo[s], q0));
+          if (two) {
+            m += max(0, min(hi2[s], q1) - max(lo2[s], q0));
+            m -= max(0, min(min(hi[s], hi2[s]), q1) - max(max(lo[s], lo2[s]), q0));
+          }
           kept &= m == 0;
           masked &= m == rows;
         }
@@ -229,7 +278,8 @@ __global__ void __launch_bounds__(256) classify_ranges_kernel(const ClassifyPara
           if (c < cols) {
             vm = low_bits32(rows - 32 * w);
             word = vm & ~(low_bits32(hi[s] - r0) & ~low_bits32(lo[s] - r0));
-            if (p.causal) word &= ~low_bits32(k0 + c - r0);  // keep rows i >= j
+            if (two) word &= ~(low_bits32(hi2[s] - r0) & ~low_bits32(lo2[s] - r0));
+            if (p.causal) word &= ~low_bits32(k0 + c - p.causal_off - r0);  // keep rows i >= j - off
           }
           any |= word != 0;
           all &= word == vm;
@@ -262,9 +312,12 @@ __global__ void __launch_bounds__(256) classify_ranges_kernel(const ClassifyPara
 }
 
 cudaError_t launch_classify(const ClassifyParams& p, cudaStream_t stream) {
-  if (p.mask_kind == FDMA_MASK_DENSE) {
+  if (p.mask_kind == FDMA_MASK_DENSE || p.mask_kind == FDMA_MASK_DENSE_U8) {
     dim3 grid(p.nTk, p.nTq, p.B * p.Hkv);
-    classify_dense_kernel<<<grid, 256, 0, stream>>>(p);
+    if (p.mask_kind == FDMA_MASK_DENSE_U8)
+      classify_dense_kernel<true><<<grid, 256, 0, stream>>>(p);
+    else
+      classify_dense_kernel<false><<<grid, 256, 0, stream>>>(p);
   } else {
     const int64_t warps = static_cast<int64_t>(p.B) * p.Hkv * p.nTk * ((p.nTq + kRangeChunk - 1) / kRangeChunk);
     classify_ranges_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(p);

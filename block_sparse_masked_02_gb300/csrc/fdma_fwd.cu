@@ -164,7 +164,8 @@ __global__ void __launch_bounds__(192, 1)
           mbar_arrive_expect_tx(&bars[kBFull + s], L::kBB);
 #pragma unroll
           for (int c = 0; c < 2; ++c)
-            tma_load_4d_hint(sB + s * L::kBB + c * 16384, &tmB, &bars[kBFull + s], k0 + c * 64, q0, g, b, bias_pol);
+            tma_load_4d_hint(sB + s * L::kBB + c * 16384, &tmB, &bars[kBFull + s], k0 + c * 64, q0, g * p.bias_hsel,
+                             b * p.bias_bsel, bias_pol);
         }
         if (!mbar_wait(&bars[kVEmpty + s], ph, p.err, kDevErrTimeout, abort_flag)) break;
         mbar_arrive_expect_tx(&bars[kVFull + s], L::kQB);
@@ -520,7 +521,8 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
           mbar_arrive_expect_tx(&bars[k2BFull + sb], L::kBB);
 #pragma unroll
           for (int c = 0; c < 2; ++c)
-            tma_load_4d_hint(sB + sb * L::kBB + c * 16384, &tmB, &bars[k2BFull + sb], k0 + c * 64, q0, g, b, bias_pol);
+            tma_load_4d_hint(sB + sb * L::kBB + c * 16384, &tmB, &bars[k2BFull + sb], k0 + c * 64, q0, g * p.bias_hsel,
+                             b * p.bias_bsel, bias_pol);
         }
         // V_n
         {

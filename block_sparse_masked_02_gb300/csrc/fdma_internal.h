@@ -25,7 +25,9 @@ constexpr int kDevErrAlign = FDMA_ERR_CUDA;
 struct ClassifyParams {
   int B, Nq, Nk, Hkv, nTq, nTk;
   int mask_kind, causal, no_skip;
+  int causal_off;  // Nk - Nq: key j is visible from query i when j <= i + causal_off
   const uint16_t* mask;
+  const uint8_t* mask_u8;  // same buffer, FDMA_MASK_DENSE_U8
   int64_t ms_b, ms_h, ms_r;
   const int32_t* cr;
   int64_t cr_b, cr_h;
@@ -37,6 +39,7 @@ struct ClassifyParams {
 
 struct FwdParams {
   int B, Nq, Nk, Hq, Hkv, G, nTq, nTk;
+  int bias_bsel, bias_hsel;  // 0 where the bias is broadcast over batch / kv head (TMA coordinate 0)
   float scale_log2;  // scale * log2(e)
   const int8_t* kmap;
   const uint4* bits_row;
@@ -57,6 +60,7 @@ struct BwdPreParams {
 
 struct BwdParams {
   int B, Nq, Nk, Hq, Hkv, G, nTq, nTk, nqpad;
+  int bias_bsel, bias_hsel;  // 0 where the bias is broadcast over batch / kv head (TMA coordinate 0)
   float scale, scale_log2;
   const int8_t* kmap;
   const uint4* bits_col;

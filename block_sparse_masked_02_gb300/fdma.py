@@ -25,6 +25,8 @@ FDMA_ERR_WORKSPACE = 5
 FDMA_MASK_NONE = 0
 FDMA_MASK_DENSE = 1
 FDMA_MASK_COLRANGES = 2
+FDMA_MASK_DENSE_U8 = 3
+FDMA_MASK_COLRANGES2 = 4
 
 FDMA_FLAG_REUSE_CLASSIFICATION = 1
 FDMA_FLAG_NO_SKIP = 2
@@ -116,7 +118,9 @@ def _stream_ptr(stream) -> int:
 def make_args(q, k, v, *, mask=None, colranges=None, bias=None, causal=False, scale=None, workspace=None,
               flags=0) -> FdmaArgs:
     """Fill fdma_args from tensors: q (B,Nq,Hq,d), k/v (B,Nk,Hkv,d) with a contiguous
-    head dim; mask/bias (B,Hkv,Nq,Nk) with contiguous columns; colranges (B,Hkv,Nk,2)."""
+    head dim; mask (B,Hkv,Nq,Nk) bf16, uint8 or bool and bias (B,Hkv,Nq,Nk) bf16 with
+    contiguous columns (stride 0 broadcasts a batch or head axis); colranges int32
+    (B,Hkv,Nk,2) (one masked row range per key) or (B,Hkv,Nk,4) (two)."""
     a = FdmaArgs()
     a.B, a.Nq, a.Hq, a.d = (int(x) for x in q.shape)
     a.Nk, a.Hkv = int(k.shape[1]), int(k.shape[2])
@@ -128,15 +132,17 @@ def make_args(q, k, v, *, mask=None, colranges=None, bias=None, causal=False, sc
     if mask is not None and colranges is not None:
         raise ValueError("pass either mask or colranges")
     if mask is not None:
-        if mask.dtype != torch.bfloat16 or mask.stride(3) != 1:
-            raise ValueError("mask must be bf16 with contiguous columns")
-        a.mask_kind = FDMA_MASK_DENSE
+        if mask.dtype not in (torch.bfloat16, torch.uint8, torch.bool) or mask.stride(3) != 1:
+            raise ValueError("mask must be bf16, uint8 or bool with contiguous columns")
+        a.mask_kind = FDMA_MASK_DENSE if mask.dtype == torch.bfloat16 else FDMA_MASK_DENSE_U8
         a.mask = mask.data_ptr()
         a.mask_stride[:] = [mask.stride(0), mask.stride(1), mask.stride(2)]
     elif colranges is not None:
-        if colranges.dtype != torch.int32 or colranges.stride(3) != 1 or colranges.stride(2) != 2:
-            raise ValueError("colranges must be int32 with a contiguous (Nk, 2) block per head")
-        a.mask_kind = FDMA_MASK_COLRANGES
+        per = int(colranges.shape[3])
+        if colranges.dtype != torch.int32 or per not in (2, 4) or colranges.stride(3) != 1 or \
+                colranges.stride(2) != per:
+            raise ValueError("colranges must be int32 with a contiguous (Nk, 2) or (Nk, 4) block per head")
+        a.mask_kind = FDMA_MASK_COLRANGES if per == 2 else FDMA_MASK_COLRANGES2
         a.colranges = colranges.data_ptr()
         a.cr_stride[:] = [colranges.stride(0), colranges.stride(1)]
     else:

@@ -59,13 +59,19 @@ extern "C" {
 typedef enum {
   FDMA_OK = 0,
   FDMA_ERR_INVALID = 1,      /* bad argument (shape, pointer, stride, scale) */
-  FDMA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head dim, alignment, causal with Nq != Nk) */
+  FDMA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head dim, alignment, strides) */
   FDMA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
   FDMA_ERR_TIMEOUT = 4,      /* a bounded in-kernel wait expired (see fdma_get_device_error) */
   FDMA_ERR_WORKSPACE = 5     /* workspace missing or smaller than fdma_workspace_size() */
 } fdma_status;
 
-typedef enum { FDMA_MASK_NONE = 0, FDMA_MASK_DENSE = 1, FDMA_MASK_COLRANGES = 2 } fdma_mask_kind;
+typedef enum {
+  FDMA_MASK_NONE = 0,
+  FDMA_MASK_DENSE = 1,       /* bf16 (B,Hkv,Nq,Nk), nonzero = keep */
+  FDMA_MASK_COLRANGES = 2,   /* int32 (B,Hkv,Nk,2): one masked query-row range per key column */
+  FDMA_MASK_DENSE_U8 = 3,    /* uint8 / bool (B,Hkv,Nq,Nk), nonzero = keep */
+  FDMA_MASK_COLRANGES2 = 4   /* int32 (B,Hkv,Nk,4): two masked query-row ranges per key column */
+} fdma_mask_kind;
 
 /* flags */
 #define FDMA_FLAG_REUSE_CLASSIFICATION 1u /* workspace already classified for this mask: skip the classifier */
@@ -86,24 +92,31 @@ typedef struct fdma_args {
 
   /* mask selection (fdma_mask_kind) */
   int32_t mask_kind;
-  /* FDMA_MASK_DENSE: bf16 (B,Hkv,Nq,Nk), nonzero = keep; strides (batch, head, row) in elements,
-     columns contiguous; every stride a multiple of 8 elements, base 16-byte aligned
-     (else FDMA_ERR_UNSUPPORTED). */
+  /* FDMA_MASK_DENSE: bf16 (B,Hkv,Nq,Nk), nonzero = keep (both signed zeros count as zero).
+     FDMA_MASK_DENSE_U8: uint8 (or bool) (B,Hkv,Nq,Nk), nonzero = keep.
+     Strides (batch, head, row) in elements, columns contiguous; every stride a multiple of 8
+     elements (0 broadcasts a batch or head), base 16-byte aligned (else FDMA_ERR_UNSUPPORTED). */
   const void* mask;
   int64_t mask_stride[3];
   /* FDMA_MASK_COLRANGES: int32 (B,Hkv,Nk,2): query rows [start,end) are MASKED for key
      column j (start >= end: none masked; values outside [0,Nq) are clamped by the test).
+     FDMA_MASK_COLRANGES2: int32 (B,Hkv,Nk,4): rows [start1,end1) and [start2,end2) are
+     masked (the union), each range read as above.
      cr_stride = (batch, head) strides in int32 elements; within one (batch, head) the
-     (Nk, 2) block is contiguous (key j at offset 2*j). */
+     (Nk, 2) or (Nk, 4) block is contiguous (key j at offset 2*j or 4*j). */
   const int32_t* colranges;
   int64_t cr_stride[2];
 
   /* optional bf16 bias (B,Hkv,Nq,Nk) (NULL = zero bias); strides (batch, head, row) in
-     elements; row stride a multiple of 8 elements, base 16-byte aligned. */
+     elements, each a multiple of 8 elements, base 16-byte aligned.  A batch or head stride
+     of 0 broadcasts the bias over that axis (the row stride must be nonzero); dBias is
+     still returned per (batch, kv head): sum it over a broadcast axis for the gradient of
+     the broadcast tensor. */
   const void* bias;
   int64_t bias_stride[3];
 
-  int32_t is_causal; /* 1: keep additionally requires j <= i (requires Nq == Nk) */
+  int32_t is_causal; /* 1: keep additionally requires j <= i + (Nk - Nq) (bottom-right aligned:
+                        j <= i when Nq == Nk; rows that see no key are fully masked) */
   float scale;       /* multiplies Q K^T only; must be finite and > 0 */
   uint32_t flags;    /* FDMA_FLAG_* */
 

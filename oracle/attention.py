@@ -11,10 +11,13 @@ Definition followed (Flash-DMA README, "Quick Start" example and
 "Key Features"; Flash-DMA issue #73, "Project Progress"; FlashMask README,
 "Formulation"):
 
-    keep(b,g,i,j) = mask[b,g,i,j] != 0            (dense 4D mask, per kv head)
-                  | not (start[b,g,j] <= i < end[b,g,j])   (column ranges)
+    keep(b,g,i,j) = mask[b,g,i,j] != 0            (dense 4D mask, per kv head; bf16, uint8 or bool)
+                  | not (start[b,g,j] <= i < end[b,g,j])   (column ranges: one masked
+                                                            row range per key column,
+                                                            or two, masked as a union)
                   | True                                    (no mask)
-                  and (j <= i if causal)
+                  and (j <= i + Nk - Nq if causal)          (bottom-right aligned; j <= i
+                                                            for square problems)
     s_ij = scale * q_i . k_j + bias[b,g,i,j]   if keep, else -inf
     P    = softmax_j(s),  O_i = sum_j P_ij v_j,  lse_i = max_j s_ij + ln sum_j exp(s_ij - max)
 
@@ -68,7 +71,7 @@ class Problem:
     """Inputs of one attention call, as given to both implementations.
 
     q (B,Nq,Hq,d), k/v (B,Nk,Hkv,d), dout like q; bias and mask (B,Hkv,Nq,Nk)
-    or None; colranges (B,Hkv,Nk,2) int or None.  Tensors may be torch (any
+    or None; colranges (B,Hkv,Nk,2) or (B,Hkv,Nk,4) int or None.  Tensors may be torch (any
     dtype, any device) or numpy; slices are converted to float64 on demand.
     """
 
@@ -93,13 +96,15 @@ def keep_rows(p: Problem, b: int, g: int, r0: int, r1: int) -> np.ndarray:
     if p.mask is not None:
         keep = _f64(p.mask[b, g, r0:r1, :]) != 0.0
     elif p.colranges is not None:
-        cr = _i64(p.colranges[b, g])  # (Nk, 2)
-        start, end = cr[:, 0][None, :], cr[:, 1][None, :]
-        keep = ~((start <= i) & (i < end))
+        cr = _i64(p.colranges[b, g])  # (Nk, 2) or (Nk, 4)
+        masked = (cr[:, 0][None, :] <= i) & (i < cr[:, 1][None, :])
+        if cr.shape[1] == 4:
+            masked |= (cr[:, 2][None, :] <= i) & (i < cr[:, 3][None, :])
+        keep = ~masked
     else:
         keep = np.ones((r1 - r0, p.Nk), dtype=bool)
     if p.causal:
-        keep = keep & (j <= i)
+        keep = keep & (j <= i + (p.Nk - p.Nq))
     return keep
 
 

@@ -160,6 +160,65 @@ def test_colranges_ragged_causal(F, flags):
     run_and_compare(F, inp, True, 0.125, flags=flags)
 
 
+@pytest.mark.parametrize("Nq,Nk,d", [(200, 392, 64), (392, 200, 128), (296, 296, 128)])
+def test_bottom_right_causal_rectangular(F, Nq, Nk, d):
+    """Causal with Nq != Nk is bottom-right aligned (j <= i + Nk - Nq); with Nq > Nk
+    the first Nq - Nk rows see no key."""
+    g = torch.Generator().manual_seed(31 + Nq)
+    B, Hq, Hkv = 2, 4, 2
+    inp = dict(q=torch.randn(B, Nq, Hq, d, generator=g).bfloat16(), k=torch.randn(B, Nk, Hkv, d, generator=g).bfloat16(),
+               v=torch.randn(B, Nk, Hkv, d, generator=g).bfloat16(),
+               dout=torch.randn(B, Nq, Hq, d, generator=g).bfloat16(),
+               bias=torch.randn(B, Hkv, Nq, Nk, generator=g).bfloat16(),
+               mask=(torch.rand(B, Hkv, Nq, Nk, generator=g) < 0.6).bfloat16())
+    run_and_compare(F, inp, True, 0.11)
+
+
+@pytest.mark.parametrize("dtype", [torch.uint8, torch.bool])
+def test_uint8_and_bool_masks(F, dtype):
+    """A uint8 / bool mask gives the same tiles and results as the bf16 mask with the
+    same zeros (nonzero = keep)."""
+    wl = W.scaled(W.WORKLOADS["n4096_hq32_hkv8"], Nq=392, Nk=392, Hq=4, Hkv=2, keep_window=96, seed=27)
+    inp = W.make_inputs(wl)
+    m8 = (inp["mask"] != 0).to(torch.uint8) * 3 if dtype == torch.uint8 else (inp["mask"] != 0)
+    alt = dict(inp, mask=m8)
+    run_and_compare(F, alt, True, wl.scale)
+    q, k, v, bias = (inp[n].cuda() for n in ("q", "k", "v", "bias"))
+    a = F.fwd(q, k, v, mask=inp["mask"].cuda(), bias=bias, causal=True, scale=wl.scale)
+    b = F.fwd(q, k, v, mask=m8.cuda(), bias=bias, causal=True, scale=wl.scale)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    assert torch.equal(F.classify_blocks(q, k, v, mask=inp["mask"].cuda(), causal=True),
+                       F.classify_blocks(q, k, v, mask=m8.cuda(), causal=True))
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_two_column_ranges(F, causal):
+    g = torch.Generator().manual_seed(33)
+    B, N, Hq, Hkv, d = 2, 300, 4, 2, 128
+    rs = []
+    for _ in range(2):
+        s0 = torch.randint(-5, N, (B, Hkv, N), generator=g)
+        rs.append(torch.stack([s0, s0 + torch.randint(-10, 120, (B, Hkv, N), generator=g)], -1))
+    cr = torch.cat(rs, -1).to(torch.int32).contiguous()
+    cr[0, 1, 128:256] = torch.tensor([0, 150, 140, N], dtype=torch.int32)  # a key tile masked for every row
+    inp = dict(q=torch.randn(B, N, Hq, d, generator=g).bfloat16(), k=torch.randn(B, N, Hkv, d, generator=g).bfloat16(),
+               v=torch.randn(B, N, Hkv, d, generator=g).bfloat16(),
+               dout=torch.randn(B, N, Hq, d, generator=g).bfloat16(), colranges=cr)
+    run_and_compare(F, inp, causal, 0.1)
+
+
+def test_broadcast_bias(F):
+    """A bias broadcast over batch and kv heads (strides 0); dBias is per (batch, kv head)."""
+    g = torch.Generator().manual_seed(35)
+    B, N, Hq, Hkv, d = 2, 256, 4, 2, 64
+    bias = torch.randn(1, 1, N, N, generator=g).bfloat16().expand(B, Hkv, N, N)
+    mask = (torch.rand(B, Hkv, N, N, generator=g) < 0.5).bfloat16()
+    inp = dict(q=torch.randn(B, N, Hq, d, generator=g).bfloat16(), k=torch.randn(B, N, Hkv, d, generator=g).bfloat16(),
+               v=torch.randn(B, N, Hkv, d, generator=g).bfloat16(),
+               dout=torch.randn(B, N, Hq, d, generator=g).bfloat16(), bias=bias, mask=mask)
+    run_and_compare(F, inp, True, 0.125)
+
+
 def test_bias_without_dbias(F):
     wl = W.scaled(W.WORKLOADS["tiny_n256_d64"], seed=4)
     run_and_compare(F, W.make_inputs(wl), True, wl.scale, want_dbias=False)
@@ -181,11 +240,17 @@ def test_no_skip_flag_changes_nothing(F):
         assert rel_l2(x.float().cpu().numpy(), y.float().cpu().numpy()) <= 1e-2
 
 
-@pytest.mark.parametrize("case", ["causal_topk", "ragged_rect", "colranges", "nomask_causal", "empty"])
+@pytest.mark.parametrize("case", ["causal_topk", "ragged_rect", "colranges", "nomask_causal", "empty", "u8_causal_rect",
+                                  "colranges2_causal", "causal_rect_wide"])
 def test_block_map_bit_exact(F, case):
     g = torch.Generator().manual_seed(21)
-    causal = case in ("causal_topk", "colranges", "nomask_causal")
+    causal = case in ("causal_topk", "colranges", "nomask_causal", "u8_causal_rect", "colranges2_causal",
+                      "causal_rect_wide")
     Nq, Nk = (328, 328) if causal else (200, 520)
+    if case == "u8_causal_rect":
+        Nq, Nk = 520, 200
+    elif case == "causal_rect_wide":
+        Nq, Nk = 200, 520
     Hkv = 2
     q = torch.randn(2, Nq, 4, 64, generator=g).bfloat16()
     k = torch.randn(2, Nk, Hkv, 64, generator=g).bfloat16()
@@ -201,6 +266,15 @@ def test_block_map_bit_exact(F, case):
         cr = W.doc_colranges(2, Hkv, Nk, 30, 150, 5)
     elif case == "empty":
         mask = torch.zeros(2, Hkv, Nq, Nk).bfloat16()
+    elif case == "u8_causal_rect":
+        mask = (torch.rand(2, Hkv, Nq, Nk, generator=g) < 0.01).to(torch.uint8)
+        mask[1, 0] = 1
+    elif case == "colranges2_causal":
+        a = W.doc_colranges(2, Hkv, Nk, 30, 150, 5)
+        b = W.doc_colranges(2, Hkv, Nk, 20, 90, 6)
+        cr = torch.cat([a, b], -1).contiguous()
+    elif case == "causal_rect_wide":
+        mask = (torch.rand(2, Hkv, Nq, Nk, generator=g) < 0.3).bfloat16()
     bm = F.classify_blocks(q.cuda(), k.cuda(), k.cuda(), mask=_cuda(mask), colranges=_cuda(cr), causal=causal)
     p = orc.Problem(q, k, k, mask=mask, colranges=cr, causal=causal)
     ref = orc.classify_blocks(p)
@@ -242,7 +316,8 @@ def test_argument_errors(F):
     with pytest.raises(F.FdmaError) as e:
         F.fwd(q96, k96, k96)
     assert e.value.status == F.FDMA_ERR_UNSUPPORTED
+    # mask rows are read 8 elements at a time: a row stride of 132 elements is refused
+    m132 = torch.ones(1, 1, 128, 132, dtype=torch.bfloat16, device="cuda")[..., :128]
     with pytest.raises(F.FdmaError) as e:
-        F.fwd(q, torch.zeros(1, 256, 1, 64, dtype=torch.bfloat16, device="cuda"),
-              torch.zeros(1, 256, 1, 64, dtype=torch.bfloat16, device="cuda"), causal=True)
+        F.fwd(q, k, k, mask=m132, causal=True)
     assert e.value.status == F.FDMA_ERR_UNSUPPORTED

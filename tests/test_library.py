@@ -75,12 +75,10 @@ def test_workspace_size_arithmetic(F):
 
 @pytest.mark.parametrize("field,value,status", [
     ("scale", float("nan"), 1), ("scale", -1.0, 1), ("Hq", 3, 1), ("d", 96, 2), ("Nk", 0, 1),
-    ("mask_kind", 7, 1), ("mask_kind", 1, 1), ("is_causal", 1, 2),
+    ("mask_kind", 7, 1), ("mask_kind", 1, 1), ("mask_kind", 3, 1), ("mask_kind", 4, 1), ("Hkv", 0, 1),
 ])
 def test_argument_validation_before_any_cuda_call(F, field, value, status):
     a = _args(F, **{field: value})
-    if field == "is_causal":
-        a.Nk = 384
     lib = F.load()
     rc = lib.fdma_fwd(ctypes.byref(a), 1 << 20, 1 << 20, None)
     assert rc == status

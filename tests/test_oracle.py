@@ -97,6 +97,44 @@ def test_matches_torch_sdpa(Hq, Hkv, causal, with_mask):
         assert np.abs(a - b).max() < 1e-10 * max(1.0, np.abs(b).max())
 
 
+@pytest.mark.parametrize("Nq,Nk", [(37, 70), (70, 37), (64, 64)])
+def test_bottom_right_causal_matches_torch_lower_right_bias(Nq, Nk):
+    """Causal alignment when Nq != Nk: torch's own lower-right causal bias
+    (torch.nn.attention.bias.causal_lower_right) decides which keys a row sees."""
+    from torch.nn.attention.bias import causal_lower_right
+
+    p = _problem(41, B=2, Nq=Nq, Nk=Nk, Hq=4, Hkv=2, d=8, causal=True, mask="dense", density=0.8, scale=0.4)
+    O, lse = orc.forward(p)
+    dq, dk, dv, dbias = orc.backward(p)
+    G = p.G
+    q = p.q.permute(0, 2, 1, 3).clone().requires_grad_(True)
+    k = p.k.permute(0, 2, 1, 3).clone().requires_grad_(True)
+    v = p.v.permute(0, 2, 1, 3).clone().requires_grad_(True)
+    bias = p.bias.clone().requires_grad_(True)
+    keep = (p.mask != 0) & causal_lower_right(Nq, Nk)._materialize()
+    # rows with no kept key are O = 0 / no gradient in the oracle; SDPA makes them NaN, so
+    # they are compared separately and their dO is zeroed for the library run
+    live = keep.any(dim=-1)  # (B, Hkv, Nq)
+    am = bias.masked_fill(~keep, float("-inf"))
+    am = am.masked_fill(~live[..., None], 0.0).repeat_interleave(G, dim=1)
+    out = torch.nn.functional.scaled_dot_product_attention(
+        q, k.repeat_interleave(G, dim=1), v.repeat_interleave(G, dim=1), attn_mask=am, scale=p.scale)
+    live_h = live.repeat_interleave(G, dim=1)  # (B, Hq, Nq)
+    do = p.dout.permute(0, 2, 1, 3) * live_h[..., None]
+    (out * do).sum().backward()
+    rO = out.detach().permute(0, 2, 1, 3).numpy()
+    lv = live_h.permute(0, 2, 1).numpy()  # (B, Nq, Hq)
+    assert np.abs(O[lv] - rO[lv]).max() < 1e-10
+    assert np.all(O[~lv] == 0.0) and np.all(np.isneginf(lse.transpose(0, 2, 1)[~lv]))
+    if Nq > Nk:
+        assert (~lv).any()  # the first Nq - Nk rows see no key
+    for a, b in ((dq, q.grad.permute(0, 2, 1, 3).numpy()), (dk, k.grad.permute(0, 2, 1, 3).numpy()),
+                 (dv, v.grad.permute(0, 2, 1, 3).numpy())):
+        assert np.abs(a - b).max() < 1e-10 * max(1.0, np.abs(b).max())
+    rdb = bias.grad.masked_fill(~live[..., None], 0.0).numpy()
+    assert np.abs(dbias - rdb).max() < 1e-10 * max(1.0, np.abs(rdb).max())
+
+
 def test_all_ones_mask_zero_bias_is_plain_softmax_attention():
     p = _problem(3, B=1, Nq=50, Nk=50, Hq=2, Hkv=2, d=8, causal=False, mask=None, bias=False)
     O, lse = orc.forward(p)
@@ -240,10 +278,62 @@ def test_colranges_equal_dense_expansion():
     assert np.array_equal(orc.classify_blocks(p, 8, 8), orc.classify_blocks(d, 8, 8))
 
 
+def test_two_column_ranges_are_the_intersection_of_single_ranges():
+    """Two masked row ranges per key column keep exactly what both single-range
+    masks keep (the union of the masked ranges), and an empty second range changes
+    nothing."""
+    g = torch.Generator().manual_seed(17)
+    B, N, Hkv = 2, 41, 2
+    base = _problem(19, B=B, Nq=N, Nk=N, Hq=4, Hkv=Hkv, d=4, causal=True, mask=None)
+    r = []
+    for _ in range(2):
+        s0 = torch.randint(-3, N + 3, (B, Hkv, N), generator=g)
+        r.append(torch.stack([s0, s0 + torch.randint(-2, N // 2, (B, Hkv, N), generator=g)], dim=-1))
+    cr2 = torch.cat(r, dim=-1).to(torch.int32)
+
+    def with_cr(cr):
+        return orc.Problem(base.q, base.k, base.v, bias=base.bias, colranges=cr, causal=True, scale=base.scale,
+                           dout=base.dout)
+
+    k1 = np.stack([np.stack([orc.keep_rows(with_cr(r[0].to(torch.int32)), b, h, 0, N) for h in range(Hkv)])
+                   for b in range(B)])
+    k2 = np.stack([np.stack([orc.keep_rows(with_cr(r[1].to(torch.int32)), b, h, 0, N) for h in range(Hkv)])
+                   for b in range(B)])
+    dense = orc.Problem(base.q, base.k, base.v, bias=base.bias, mask=torch.from_numpy((k1 & k2).astype(np.float64)),
+                        causal=True, scale=base.scale, dout=base.dout)
+    two = with_cr(cr2)
+    a, b = orc.forward(two), orc.forward(dense)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    for x, y in zip(orc.backward(two), orc.backward(dense)):
+        assert np.array_equal(x, y)
+    assert np.array_equal(orc.classify_blocks(two, 8, 8), orc.classify_blocks(dense, 8, 8))
+    empty2 = torch.cat([r[0], torch.zeros_like(r[0])], dim=-1).to(torch.int32)
+    assert np.array_equal(orc.forward(with_cr(empty2))[0], orc.forward(with_cr(r[0].to(torch.int32)))[0])
+
+
+def test_uint8_and_bool_masks_equal_the_bf16_mask():
+    p = _problem(23, B=1, Nq=33, Nk=33, Hq=2, Hkv=1, d=4, causal=True, mask="dense", density=0.4)
+    ref = orc.forward(p)
+    for m in (p.mask.to(torch.uint8) * 7, p.mask != 0):
+        o = orc.forward(orc.Problem(p.q, p.k, p.v, bias=p.bias, mask=m, causal=True, scale=p.scale))
+        assert np.array_equal(o[0], ref[0]) and np.array_equal(o[1], ref[1])
+
+
+def test_broadcast_bias_equals_the_materialised_bias():
+    p = _problem(29, B=2, Nq=24, Nk=24, Hq=4, Hkv=2, d=4, causal=True, mask="dense", density=0.7)
+    bb = torch.randn(1, 1, 24, 24, generator=torch.Generator().manual_seed(5), dtype=torch.float64)
+    exp = bb.expand(2, 2, 24, 24)  # stride 0 over batch and heads
+    a = orc.Problem(p.q, p.k, p.v, bias=exp, mask=p.mask, causal=True, scale=p.scale, dout=p.dout)
+    b = orc.Problem(p.q, p.k, p.v, bias=exp.contiguous(), mask=p.mask, causal=True, scale=p.scale, dout=p.dout)
+    for x, y in zip(orc.forward(a) + orc.backward(a), orc.forward(b) + orc.backward(b)):
+        assert np.array_equal(x, y)
+
+
 # ----------------------------------------------------------------- block map
-@pytest.mark.parametrize("Nq,Nk,tm,tn,causal", [(13, 11, 4, 5, True), (17, 17, 8, 8, False), (20, 9, 3, 4, False)])
+@pytest.mark.parametrize("Nq,Nk,tm,tn,causal", [(13, 11, 4, 5, True), (17, 17, 8, 8, False), (20, 9, 3, 4, False),
+                                                 (9, 20, 4, 3, True), (17, 17, 8, 8, True)])
 def test_block_map_brute_force(Nq, Nk, tm, tn, causal):
-    p = _problem(12, B=1, Nq=Nq, Nk=Nk, Hq=2, Hkv=2, d=2, causal=causal and Nq == Nk, mask="dense", density=0.15)
+    p = _problem(12, B=1, Nq=Nq, Nk=Nk, Hq=2, Hkv=2, d=2, causal=causal, mask="dense", density=0.15)
     p.mask[0, 1, :tm, :] = 1.0  # a band of full tiles
     bm = orc.classify_blocks(p, tm, tn)
     mask = orc._f64(p.mask)
@@ -254,7 +344,7 @@ def test_block_map_brute_force(Nq, Nk, tm, tn, causal):
                 for i in range(qt * tm, min((qt + 1) * tm, Nq)):
                     for j in range(kt * tn, min((kt + 1) * tn, Nk)):
                         n += 1
-                        kept += int(mask[0, g, i, j] != 0 and (not p.causal or j <= i))
+                        kept += int(mask[0, g, i, j] != 0 and (not p.causal or j <= i + Nk - Nq))
                 ref = 0 if kept == 0 else (2 if kept == n else 1)
                 assert bm[0, g, qt, kt] == ref
 
