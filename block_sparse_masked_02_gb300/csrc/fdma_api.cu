@@ -242,6 +242,7 @@ int fdma_fwd(const fdma_args* a, void* out, float* lse, void* stream_v) {
   p.G = a->Hq / a->Hkv;
   p.nTq = cdiv(a->Nq, kTile);
   p.nTk = cdiv(a->Nk, kTile);
+  p.scale = a->scale;
   p.scale_log2 = a->scale * 1.4426950408889634f;
   p.bias_bsel = a->bias_stride[0] == 0 ? 0 : 1;
   p.bias_hsel = a->bias_stride[1] == 0 ? 0 : 1;

@@ -71,10 +71,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
   for (int c = lane * 4; c < p.d; c += 128) *reinterpret_cast<float4*>(dq + c) = make_float4(0.f, 0.f, 0.f, 0.f);
   if (lane == 0) {
     const int64_t o = (static_cast<int64_t>(b) * p.Hq + h) * p.nqpad + i;
-    float l2 = kPosInf;
+    float l2 = -kPosInf;
     if (valid) {
       const float l = p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + i];
-      l2 = (l == -kPosInf) ? kPosInf : l * kLog2e;
+      l2 = (l == -kPosInf) ? -kPosInf : -(l * kLog2e);
     }
     p.lse2[o] = l2;
     p.delta[o] = valid ? acc : 0.f;
@@ -359,9 +359,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool kin = kidx < p.Nk;
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
     const int qbase = wg * 64;
-    float acc[WANT_DBIAS ? 64 : 1];
+    uint64_t acc2[WANT_DBIAS ? 32 : 1];  // dBias partial sums, pairs of queries
 #pragma unroll
-    for (int c = 0; c < (WANT_DBIAS ? 64 : 1); ++c) acc[c] = 0.f;
+    for (int c = 0; c < (WANT_DBIAS ? 32 : 1); ++c) acc2[c] = 0ull;
+    const uint64_t sc2 = f2(p.scale_log2, p.scale_log2);
+    const uint64_t lg2 = f2(kLog2e, kLog2e);
     int n = 0, qi_count = 0;
     bool ok = true;
     // No compute thread leaves these loops early, so every one of them reaches every named
@@ -409,36 +411,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint32_t sr[16], dr[16];
           tmem_ld16(tl + col, sr);
           tmem_ld16(tl + 128 + col, dr);
-          float l16[16], d16[16];  // this chunk's 16 lse / delta values (broadcast 16-byte reads)
+          uint64_t nl[8], dd[8];  // this chunk's 16 -lse2 / delta values as pairs (broadcast 16-byte reads)
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
-            const float4 a = reinterpret_cast<const float4*>(lse2 + c * 16)[v];
-            const float4 bq = reinterpret_cast<const float4*>(dlt + c * 16)[v];
-            l16[4 * v] = a.x; l16[4 * v + 1] = a.y; l16[4 * v + 2] = a.z; l16[4 * v + 3] = a.w;
-            d16[4 * v] = bq.x; d16[4 * v + 1] = bq.y; d16[4 * v + 2] = bq.z; d16[4 * v + 3] = bq.w;
+            const ulonglong2 a = reinterpret_cast<const ulonglong2*>(lse2 + c * 16)[v];
+            const ulonglong2 bq = reinterpret_cast<const ulonglong2*>(dlt + c * 16)[v];
+            nl[2 * v] = a.x; nl[2 * v + 1] = a.y;
+            dd[2 * v] = bq.x; dd[2 * v + 1] = bq.y;
           }
           tmem_ld_wait();
           const uint32_t word = c < 2 ? bw0 : bw1;
           uint32_t pk[8], dk[8];
 #pragma unroll
           for (int e = 0; e < 16; e += 2) {
-            float pv[2], dv[2];
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              const int qi = c * 16 + e + t;  // 0..63 within this half
-              const bool keep = (word >> (qi & 31)) & 1u;
-              float bval = 0.f;
-              if (HAS_BIAS) {
-                const uint32_t w2 = bpk[qi >> 1];
-                bval = __uint_as_float((qi & 1) ? (w2 & 0xFFFF0000u) : (w2 << 16));
-              }
-              const float x = fmaf(__uint_as_float(sr[e + t]), p.scale_log2, fmaf(bval, kLog2e, -l16[e + t]));
-              pv[t] = keep ? ex2(x) : 0.f;
-              dv[t] = pv[t] * (__uint_as_float(dr[e + t]) - d16[e + t]);
-              if (WANT_DBIAS) acc[qi] += dv[t];
-            }
-            pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
-            dk[e >> 1] = pack_bf16x2(dv[0], dv[1]);
+            const int qi = c * 16 + e;  // 0..63 within this half (even)
+            const uint64_t s2 = f2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+            const uint64_t x2 = HAS_BIAS ? fma2(s2, sc2, fma2(bf16x2_to_f2(bpk[qi >> 1]), lg2, nl[e >> 1]))
+                                         : fma2(s2, sc2, nl[e >> 1]);
+            float x0, x1;
+            f2split(x2, x0, x1);
+            const float p0 = ((word >> (qi & 31)) & 1u) ? ex2(x0) : 0.f;
+            const float p1 = ((word >> ((qi + 1) & 31)) & 1u) ? ex2(x1) : 0.f;
+            const uint64_t dv2 =
+                mul2(f2(p0, p1), sub2(f2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), dd[e >> 1]));
+            if (WANT_DBIAS) acc2[qi >> 1] = add2(acc2[qi >> 1], dv2);
+            float d0, d1;
+            f2split(dv2, d0, d1);
+            pk[e >> 1] = pack_bf16x2(p0, p1);
+            dk[e >> 1] = pack_bf16x2(d0, d1);
           }
           // packed P^T stays inside this warpgroup's own S^T columns (already read):
           // queries 0..63 -> cols 0..31, queries 64..127 -> cols 64..95
@@ -488,12 +488,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint8_t* dbt = sDS + (j >> 6) * 16384 + (j & 7) * 2;
         const int jc = (j & 63) >> 3;
 #pragma unroll
-        for (int qi = 0; qi < 64; ++qi) {
-          const int i = qbase + qi;
-          if (ok)
-            *reinterpret_cast<uint16_t*>(dbt + i * 128 + ((jc ^ (i & 7)) << 4)) =
-                static_cast<uint16_t>(pack_bf16x2(acc[qi], 0.f) & 0xFFFFu);
-          acc[qi] = 0.f;
+        for (int qp = 0; qp < 32; ++qp) {
+          const int i = qbase + 2 * qp;
+          float a0, a1;
+          f2split(acc2[qp], a0, a1);
+          const uint32_t w = pack_bf16x2(a0, a1);
+          if (ok) {
+            *reinterpret_cast<uint16_t*>(dbt + i * 128 + ((jc ^ (i & 7)) << 4)) = static_cast<uint16_t>(w & 0xFFFFu);
+            *reinterpret_cast<uint16_t*>(dbt + (i + 1) * 128 + ((jc ^ ((i + 1) & 7)) << 4)) =
+                static_cast<uint16_t>(w >> 16);
+          }
+          acc2[qp] = 0ull;
         }
         fence_proxy_async_smem();
         named_bar_sync(1, 256);

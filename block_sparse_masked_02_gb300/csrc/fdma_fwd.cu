@@ -619,6 +619,12 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
     const int i = q0 + r;
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
     const uint32_t scol = w * 128, ocol = 256 + w * 128;
+    // Row maximum m_ref is kept in the units of u: u = S*scale + bias with a bias, u = S
+    // without one (scale > 0); the softmax exponent in log2 units is u*cexp - m_ref*cexp.
+    const float cexp = HAS_BIAS ? kLog2e : p.scale_log2;
+    const float thr_u = kRescaleThreshold / cexp;
+    const uint64_t c2 = f2(cexp, cexp);
+    const uint64_t sc2 = f2(p.scale, p.scale);
     float m_ref = kNegInf, l = 0.f;
     int n = 0;
     bool ok = true;
@@ -629,71 +635,106 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
       const bool partial = map_row[kt] == kPartial || (ragged_k && kt == p.nTk - 1);
       uint4 bits = make_uint4(~0u, ~0u, ~0u, ~0u);
       if (partial) bits = __ldg(&p.bits_row[(tile_base + kt) * kTile + r]);
-      float x[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(tl + scol + c * 32, raw);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[c * 32 + j] = __uint_as_float(raw[j]) * p.scale_log2;
-      }
+      uint64_t u[64];  // u of keys 2t, 2t+1
       if (HAS_BIAS) {
         const int sb = n & 1;
         if (!(ok = mbar_wait(&bars[k2BFull + sb], (n >> 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
         const uint8_t* bt = sB + sb * L::kBB + r * 128;
 #pragma unroll
-        for (int cc = 0; cc < 16; ++cc) {
-          const uint4 v = *reinterpret_cast<const uint4*>(bt + (cc >> 3) * 16384 + (((cc & 7) ^ (r & 7)) << 4));
-          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(tl + scol + c * 32, raw);
+          uint4 bv[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            x[cc * 8 + 2 * e] = fmaf(__uint_as_float(wv[e] << 16), kLog2e, x[cc * 8 + 2 * e]);
-            x[cc * 8 + 2 * e + 1] = fmaf(__uint_as_float(wv[e] & 0xFFFF0000u), kLog2e, x[cc * 8 + 2 * e + 1]);
+          for (int q = 0; q < 4; ++q) {
+            const int cc = c * 4 + q;
+            bv[q] = *reinterpret_cast<const uint4*>(bt + (cc >> 3) * 16384 + (((cc & 7) ^ (r & 7)) << 4));
+          }
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t wv[4] = {bv[q].x, bv[q].y, bv[q].z, bv[q].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int t = c * 16 + q * 4 + e;
+              u[t] = fma2(f2(__uint_as_float(raw[2 * (q * 4 + e)]), __uint_as_float(raw[2 * (q * 4 + e) + 1])), sc2,
+                          bf16x2_to_f2(wv[e]));
+            }
           }
         }
         mbar_arrive(&bars[k2BEmpty + sb]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(tl + scol + c * 32, raw);
+          tmem_ld_wait();
+#pragma unroll
+          for (int t = 0; t < 16; ++t) u[c * 16 + t] = f2(__uint_as_float(raw[2 * t]), __uint_as_float(raw[2 * t + 1]));
+        }
       }
       if (partial) {
         const uint32_t bw[4] = {bits.x, bits.y, bits.z, bits.w};
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (!((bw[c >> 5] >> (c & 31)) & 1u)) x[c] = kNegInf;
+        for (int t = 0; t < 64; ++t) {
+          float u0, u1;
+          f2split(u[t], u0, u1);
+          if (!((bw[t >> 4] >> ((2 * t) & 31)) & 1u)) u0 = kNegInf;
+          if (!((bw[t >> 4] >> ((2 * t + 1) & 31)) & 1u)) u1 = kNegInf;
+          u[t] = f2(u0, u1);
+        }
       }
       float mx8[8];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) mx8[t] = x[t];
+      for (int t = 0; t < 4; ++t) f2split(u[t], mx8[2 * t], mx8[2 * t + 1]);
 #pragma unroll
-      for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int t = 4; t < 64; t += 4) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float a0, a1;
+          f2split(u[t + q], a0, a1);
+          // three-input maximum: the running value and both halves of the pair
+          asm("max.f32 %0, %0, %1, %2;" : "+f"(mx8[2 * q]) : "f"(a0), "f"(a1));
+        }
+      }
+      float mx;
+      asm("max.f32 %0, %1, %2, %3;" : "=f"(mx) : "f"(mx8[0]), "f"(mx8[2]), "f"(mx8[4]));
+      asm("max.f32 %0, %0, %1, %2;" : "+f"(mx) : "f"(mx8[6]), "f"(mx8[1]));
+      asm("max.f32 %0, %0, %1, %2;" : "+f"(mx) : "f"(mx8[3]), "f"(mx8[5]));
+      mx = fmaxf(mx, mx8[7]);
       const float m_new = fmaxf(m_ref, mx);
       float alpha = 1.f;
       bool resc = false;
-      if (m_new > m_ref + kRescaleThreshold) {
+      if (m_new > m_ref + thr_u) {
         if (m_ref == kNegInf) {
           m_ref = m_new;
         } else {
-          alpha = ex2(m_ref - m_new);
+          alpha = ex2((m_ref - m_new) * cexp);
           l *= alpha;
           m_ref = m_new;
           resc = true;
         }
       }
-      const float mu = (m_ref == kNegInf) ? 0.f : m_ref;
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      const float nm = (m_ref == kNegInf) ? 0.f : -(m_ref * cexp);
+      const uint64_t nm2 = f2(nm, nm);
+      uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const float p0 = ex2(x[c * 32 + 2 * j] - mu);
-          const float p1 = ex2(x[c * 32 + 2 * j + 1] - mu);
+          float e0, e1;
+          f2split(fma2(u[c * 16 + j], c2, nm2), e0, e1);
+          const float p0 = ex2(e0), p1 = ex2(e1);
           pk[j] = pack_bf16x2(p0, p1);
-          sum4[j & 3] += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xFFFF0000u);
+          sum2[j & 1] = add2(sum2[j & 1], bf16x2_to_f2(pk[j]));  // the row sum of P as rounded for PV
         }
         tmem_st16(tl + scol + c * 16, pk);
       }
-      l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      {
+        const uint64_t s2 = add2(sum2[0], sum2[1]);
+        float s0, s1;
+        f2split(s2, s0, s1);
+        l += s0 + s1;
+      }
       if (__any_sync(0xffffffffu, resc)) {
         // S_w(n) was issued after PV_w(n-1), so O_w is complete here; PV_w(n) is
         // issued only after the arrival below.
@@ -737,7 +778,7 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
         }
       }
       if (i < p.Nq)
-        p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + i] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : kNegInf;
+        p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + i] = l > 0.f ? (m_ref * cexp + log2f(l)) * kLn2 : kNegInf;
     }
   }
   tc_fence_before();

@@ -40,7 +40,7 @@ struct ClassifyParams {
 struct FwdParams {
   int B, Nq, Nk, Hq, Hkv, G, nTq, nTk;
   int bias_bsel, bias_hsel;  // 0 where the bias is broadcast over batch / kv head (TMA coordinate 0)
-  float scale_log2;  // scale * log2(e)
+  float scale, scale_log2;  // softmax scale and scale * log2(e)
   const int8_t* kmap;
   const uint4* bits_row;
   uint16_t* out;  // (B,Nq,Hq,d)
