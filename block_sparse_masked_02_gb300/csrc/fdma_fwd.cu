@@ -410,7 +410,7 @@ enum Fwd2Bar : int {
 };
 
 constexpr int kFwd2Threads = 384;
-constexpr uint32_t kFwd2RegsLow = 104, kFwd2RegsHigh = 200;
+constexpr uint32_t kFwd2RegsLow = 120, kFwd2RegsHigh = 192;
 constexpr int kFwd2MinLaunchRegs = (kFwd2RegsLow + 2 * kFwd2RegsHigh) / 3;  // 168
 
 template <int D, bool HAS_BIAS>
@@ -629,47 +629,49 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
     int n = 0;
     bool ok = true;
     uint32_t raw[32];
+    // The keep bits of a partial tile are fetched one active tile ahead, so their
+    // load latency overlaps the wait for S.
+    auto is_partial = [&](int kt) { return map_row[kt] == kPartial || (ragged_k && kt == p.nTk - 1); };
+    uint4 bits_next = make_uint4(~0u, ~0u, ~0u, ~0u);
+    if (first_kt < p.nTk && is_partial(first_kt)) bits_next = __ldg(&p.bits_row[(tile_base + first_kt) * kTile + r]);
     for (int kt = first_kt; kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
+      const bool partial = is_partial(kt);
+      const uint4 bits = bits_next;
+      {
+        const int kn = next_active(map_row, kt, p.nTk);
+        bits_next = make_uint4(~0u, ~0u, ~0u, ~0u);
+        if (kn < p.nTk && is_partial(kn)) bits_next = __ldg(&p.bits_row[(tile_base + kn) * kTile + r]);
+      }
       if (!(ok = mbar_wait(&bars[k2SFull + w], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
       tc_fence_after();
-      const bool partial = map_row[kt] == kPartial || (ragged_k && kt == p.nTk - 1);
-      uint4 bits = make_uint4(~0u, ~0u, ~0u, ~0u);
-      if (partial) bits = __ldg(&p.bits_row[(tile_base + kt) * kTile + r]);
       uint64_t u[64];  // u of keys 2t, 2t+1
       if (HAS_BIAS) {
         const int sb = n & 1;
         if (!(ok = mbar_wait(&bars[k2BFull + sb], (n >> 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
         const uint8_t* bt = sB + sb * L::kBB + r * 128;
+        uint32_t sraw[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(tl + scol + c * 32, raw);
-          uint4 bv[4];
+        for (int c = 0; c < 4; ++c) tmem_ld32(tl + scol + c * 32, sraw[c]);
+        tmem_ld_wait();
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int cc = c * 4 + q;
-            bv[q] = *reinterpret_cast<const uint4*>(bt + (cc >> 3) * 16384 + (((cc & 7) ^ (r & 7)) << 4));
-          }
-          tmem_ld_wait();
+        for (int cc = 0; cc < 16; ++cc) {
+          const uint4 bv = *reinterpret_cast<const uint4*>(bt + (cc >> 3) * 16384 + (((cc & 7) ^ (r & 7)) << 4));
+          const uint32_t wv[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t wv[4] = {bv[q].x, bv[q].y, bv[q].z, bv[q].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int t = c * 16 + q * 4 + e;
-              u[t] = fma2(f2(__uint_as_float(raw[2 * (q * 4 + e)]), __uint_as_float(raw[2 * (q * 4 + e) + 1])), sc2,
-                          bf16x2_to_f2(wv[e]));
-            }
+          for (int e = 0; e < 4; ++e) {
+            const int t = cc * 4 + e;
+            u[t] = fma2(f2(__uint_as_float(sraw[t >> 4][(2 * t) & 31]), __uint_as_float(sraw[t >> 4][(2 * t + 1) & 31])), sc2,
+                        bf16x2_to_f2(wv[e]));
           }
         }
         mbar_arrive(&bars[k2BEmpty + sb]);
       } else {
+        uint32_t sraw[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(tl + scol + c * 32, raw);
-          tmem_ld_wait();
+        for (int c = 0; c < 4; ++c) tmem_ld32(tl + scol + c * 32, sraw[c]);
+        tmem_ld_wait();
 #pragma unroll
-          for (int t = 0; t < 16; ++t) u[c * 16 + t] = f2(__uint_as_float(raw[2 * t]), __uint_as_float(raw[2 * t + 1]));
-        }
+        for (int t = 0; t < 64; ++t) u[t] = f2(__uint_as_float(sraw[t >> 4][(2 * t) & 31]), __uint_as_float(sraw[t >> 4][(2 * t + 1) & 31]));
       }
       if (partial) {
         const uint32_t bw[4] = {bits.x, bits.y, bits.z, bits.w};
