@@ -388,8 +388,11 @@ __global__ void __launch_bounds__(192, 1)
 // both heads read the same K, V, bias and mask tiles, which are fetched once.
 // Warps: warpgroup 0 = {TMA producer, MMA issuer, 2 idle}, warpgroup 1 =
 // softmax of head 0, warpgroup 2 = softmax of head 1 (setmaxnreg moves
-// registers to the softmax groups).  The MMA issuer interleaves
-//   PV0_{n-1}, S0_n, PV1_{n-1}, S1_n
+// registers to the softmax groups).  While a softmax warp waits for S it turns
+// the tile's bias and keep bits into an additive term (-inf where masked).  The
+// MMA issuer interleaves
+//   PV0_{n-1} (keys 0..63 as soon as their P is stored, then 64..127), S0_n,
+//   PV1_{n-1} (likewise), S1_n
 // so each head's softmax overlaps the tensor-core work of the other head, and
 // S_w(n) (written over P_w(n-1)'s columns) completes only after PV_w(n-1):
 // the softmax may rescale O_w as soon as it sees S_w(n).
@@ -403,10 +406,10 @@ enum Fwd2Bar : int {
   k2BFull = 7,     // +slot (2)
   k2BEmpty = 9,    // +slot (2)
   k2SFull = 11,    // +head (2)
-  k2PReady = 13,   // +head (2)
-  k2OFinal = 15,
-  k2Drain = 16,
-  kNumFwd2Bars = 17
+  k2PReady = 13,   // +2*head+half (4): P of keys 0..63 / 64..127 stored
+  k2OFinal = 17,
+  k2Drain = 18,
+  kNumFwd2Bars = 19
 };
 
 constexpr int kFwd2Threads = 384;
@@ -465,8 +468,7 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
     for (int i = 0; i < kNumFwd2Bars; ++i) mbar_init(&bars[i], 1);
     mbar_init(&bars[k2BEmpty + 0], 256);
     mbar_init(&bars[k2BEmpty + 1], 256);
-    mbar_init(&bars[k2PReady + 0], 128);
-    mbar_init(&bars[k2PReady + 1], 128);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars[k2PReady + i], 128);
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -558,34 +560,42 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
           umma_ss(tbase + w * 128, qd + kmajor_step(k, 128), kd + kmajor_step(k, 128), IDESC_S, k > 0);
         umma_commit(&bars[k2SFull + w]);
       };
-      auto issue_pv = [&](int w, int m) {
+      // O_w += P_w V, in two key halves, each issued once its P is stored; P of keys
+      // 16k .. 16k+15 sits in S_w's columns 8k .. 8k+7
+      auto pv_when_ready = [&](int w, int m) {
         const int sl = (2 * m + 1) % 3;
         const uint64_t vd = kvmn0 + sl * slot_step;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          umma_ts(tbase + 256 + w * 128, tbase + w * 128 + k * 8, vd + static_cast<uint64_t>((k * 2048) >> 4),
-                  IDESC_O, (m > 0 || k > 0) ? 1u : 0u);
+        for (int hf = 0; hf < 2; ++hf) {
+          if (!mbar_wait(&bars[k2PReady + 2 * w + hf], m & 1, p.err, kDevErrTimeout, abort_flag)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int k = hf * 4; k < hf * 4 + 4; ++k)
+            umma_ts(tbase + 256 + w * 128, tbase + w * 128 + k * 8, vd + static_cast<uint64_t>((k * 2048) >> 4),
+                    IDESC_O, (m > 0 || k > 0) ? 1u : 0u);
+        }
+        return true;
       };
       int n = 0;
       for (int kt = first_kt; ok && kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
         const int itk = 2 * n;
-        if (!(ok = mbar_wait(&bars[k2KvFull + itk % 3], (itk / 3) & 1, p.err, kDevErrTimeout, abort_flag))) break;
-        tc_fence_after();
         if (n == 0) {
+          if (!(ok = mbar_wait(&bars[k2KvFull + itk % 3], (itk / 3) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+          tc_fence_after();
           issue_s(0, 0);
           issue_s(1, 0);
           umma_commit(&bars[k2KvEmpty + itk % 3]);
           continue;
         }
+        // PV of the previous tile first: it needs only V_{n-1} and P, not K_n (whose
+        // ring slot frees only when the tile before that is done)
         const int m = n - 1, itv = 2 * m + 1;
         if (!(ok = mbar_wait(&bars[k2KvFull + itv % 3], (itv / 3) & 1, p.err, kDevErrTimeout, abort_flag))) break;
-        if (!(ok = mbar_wait(&bars[k2PReady + 0], m & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        if (!(ok = pv_when_ready(0, m))) break;
+        if (!(ok = mbar_wait(&bars[k2KvFull + itk % 3], (itk / 3) & 1, p.err, kDevErrTimeout, abort_flag))) break;
         tc_fence_after();
-        issue_pv(0, m);
         issue_s(0, n);
-        if (!(ok = mbar_wait(&bars[k2PReady + 1], m & 1, p.err, kDevErrTimeout, abort_flag))) break;
-        tc_fence_after();
-        issue_pv(1, m);
+        if (!(ok = pv_when_ready(1, m))) break;
         umma_commit(&bars[k2KvEmpty + itv % 3]);
         issue_s(1, n);
         umma_commit(&bars[k2KvEmpty + itk % 3]);
@@ -593,17 +603,8 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
       if (ok && n > 0) {
         const int m = n - 1, itv = 2 * m + 1;
         ok = mbar_wait(&bars[k2KvFull + itv % 3], (itv / 3) & 1, p.err, kDevErrTimeout, abort_flag) &&
-             mbar_wait(&bars[k2PReady + 0], m & 1, p.err, kDevErrTimeout, abort_flag);
-        if (ok) {
-          tc_fence_after();
-          issue_pv(0, m);
-          ok = mbar_wait(&bars[k2PReady + 1], m & 1, p.err, kDevErrTimeout, abort_flag);
-          if (ok) {
-            tc_fence_after();
-            issue_pv(1, m);
-            umma_commit(&bars[k2KvEmpty + itv % 3]);
-          }
-        }
+             pv_when_ready(0, m) && pv_when_ready(1, m);
+        if (ok) umma_commit(&bars[k2KvEmpty + itv % 3]);
       }
       umma_commit(&bars[k2OFinal]);
       umma_commit(&bars[k2Drain]);
@@ -642,36 +643,25 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
         bits_next = make_uint4(~0u, ~0u, ~0u, ~0u);
         if (kn < p.nTk && is_partial(kn)) bits_next = __ldg(&p.bits_row[(tile_base + kn) * kTile + r]);
       }
-      if (!(ok = mbar_wait(&bars[k2SFull + w], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
-      tc_fence_after();
+      // Additive term of this tile, formed while S is still being computed: the bias
+      // (u = S*scale + bias) and/or -inf at the masked keys (u = S + 0 / -inf).
+      const bool addend = HAS_BIAS || partial;
       uint64_t u[64];  // u of keys 2t, 2t+1
       if (HAS_BIAS) {
         const int sb = n & 1;
         if (!(ok = mbar_wait(&bars[k2BFull + sb], (n >> 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
         const uint8_t* bt = sB + sb * L::kBB + r * 128;
-        uint32_t sraw[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tl + scol + c * 32, sraw[c]);
-        tmem_ld_wait();
 #pragma unroll
         for (int cc = 0; cc < 16; ++cc) {
           const uint4 bv = *reinterpret_cast<const uint4*>(bt + (cc >> 3) * 16384 + (((cc & 7) ^ (r & 7)) << 4));
           const uint32_t wv[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int t = cc * 4 + e;
-            u[t] = fma2(f2(__uint_as_float(sraw[t >> 4][(2 * t) & 31]), __uint_as_float(sraw[t >> 4][(2 * t + 1) & 31])), sc2,
-                        bf16x2_to_f2(wv[e]));
-          }
+          for (int e = 0; e < 4; ++e) u[cc * 4 + e] = bf16x2_to_f2(wv[e]);
         }
         mbar_arrive(&bars[k2BEmpty + sb]);
-      } else {
-        uint32_t sraw[4][32];
+      } else if (partial) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tl + scol + c * 32, sraw[c]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int t = 0; t < 64; ++t) u[t] = f2(__uint_as_float(sraw[t >> 4][(2 * t) & 31]), __uint_as_float(sraw[t >> 4][(2 * t + 1) & 31]));
+        for (int t = 0; t < 64; ++t) u[t] = 0ull;
       }
       if (partial) {
         const uint32_t bw[4] = {bits.x, bits.y, bits.z, bits.w};
@@ -682,6 +672,19 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
           if (!((bw[t >> 4] >> ((2 * t) & 31)) & 1u)) u0 = kNegInf;
           if (!((bw[t >> 4] >> ((2 * t + 1) & 31)) & 1u)) u1 = kNegInf;
           u[t] = f2(u0, u1);
+        }
+      }
+      if (!(ok = mbar_wait(&bars[k2SFull + w], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(tl + scol + c * 32, raw);
+        tmem_ld_wait();
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const uint64_t s2 = f2(__uint_as_float(raw[2 * t]), __uint_as_float(raw[2 * t + 1]));
+          const int q = c * 16 + t;
+          u[q] = HAS_BIAS ? fma2(s2, sc2, u[q]) : (addend ? add2(s2, u[q]) : s2);
         }
       }
       float mx8[8];
@@ -715,6 +718,19 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
           resc = true;
         }
       }
+      if (__any_sync(0xffffffffu, resc)) {
+        // S_w(n) was issued after PV_w(n-1), so O_w is complete here; PV_w(n) is
+        // issued only after the arrivals below, which follow these stores.
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t o16[16];
+          tmem_ld16(tl + ocol + c * 16, o16);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) o16[j] = __float_as_uint(__uint_as_float(o16[j]) * alpha);
+          tmem_st16(tl + ocol + c * 16, o16);
+        }
+      }
       const float nm = (m_ref == kNegInf) ? 0.f : -(m_ref * cexp);
       const uint64_t nm2 = f2(nm, nm);
       uint64_t sum2[2] = {0ull, 0ull};
@@ -730,6 +746,11 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
           sum2[j & 1] = add2(sum2[j & 1], bf16x2_to_f2(pk[j]));  // the row sum of P as rounded for PV
         }
         tmem_st16(tl + scol + c * 16, pk);
+        if (c & 1) {  // keys 0..63 (c = 1), then 64..127 (c = 3): that half of PV may start
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bars[k2PReady + 2 * w + (c >> 1)]);
+        }
       }
       {
         const uint64_t s2 = add2(sum2[0], sum2[1]);
@@ -737,22 +758,6 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
         f2split(s2, s0, s1);
         l += s0 + s1;
       }
-      if (__any_sync(0xffffffffu, resc)) {
-        // S_w(n) was issued after PV_w(n-1), so O_w is complete here; PV_w(n) is
-        // issued only after the arrival below.
-#pragma unroll
-        for (int c = 0; c < D / 16; ++c) {
-          uint32_t o16[16];
-          tmem_ld16(tl + ocol + c * 16, o16);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) o16[j] = __float_as_uint(__uint_as_float(o16[j]) * alpha);
-          tmem_st16(tl + ocol + c * 16, o16);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars[k2PReady + w]);
     }
     // ------------------------------------------------------------------ epilogue
     if (ok && n > 0) ok = mbar_wait(&bars[k2OFinal], 0, p.err, kDevErrTimeout, abort_flag);
