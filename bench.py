@@ -34,9 +34,9 @@ METRIC = "effective fwd+bwd TFLOP/s (non-skipped tiles) and % of roofline, 1 GB3
 TILE = 128
 KERNELS_PER_STEP = 5  # classify, fwd, bwd_pre, bwd, dq_convert
 # DRAM bytes (read + write) of one bwd_kernel launch on this workload: an ncu capture of
-# bwd_kernel on n4096_hq32_hkv8 (360.30 MB read + 353.32 MB written) scaled by the active
+# bwd_kernel on n4096_hq32_hkv8 (332.57 MB read + 306.41 MB written) scaled by the active
 # (tile, head) units, 132096 / 16896; None whenever the kernel has changed since that capture.
-BWD_TRAFFIC_BYTES = round((360.300032e6 + 353.323264e6) * 132096 / 16896)
+BWD_TRAFFIC_BYTES = round((332.570368e6 + 306.414336e6) * 132096 / 16896)
 
 
 def _peaks():
@@ -367,7 +367,7 @@ def cpu_baseline(host, bias_win, mask_win, wl, seconds=15.0, max_tiles=None):
             "seconds": round(t_used, 3)}
 
 
-def _gpu_windows(inp, wl, tiles=16):
+def _gpu_windows(inp, wl, tiles=64):
     r0 = max(0, wl.Nq - tiles * TILE)
     host = {n: inp[n].cpu() for n in ("q", "k", "v", "dout")}
     bw = _RowWindow(inp["bias"][0, 0, r0:].cpu(), r0, inp["bias"].shape)
