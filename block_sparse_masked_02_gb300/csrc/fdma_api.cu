@@ -383,4 +383,33 @@ const char* fdma_status_string(int s) {
   }
 }
 
+int fdma_topk_mask(const void* bias, const int64_t bias_stride[3], int B, int Hkv, int Nq, int Nk, int keep_window,
+                   int mask_kind, void* mask, void* bias_out, void* stream) {
+  if (bias == nullptr || bias_stride == nullptr || mask == nullptr) return FDMA_ERR_INVALID;
+  if (B <= 0 || Hkv <= 0 || Nq <= 0 || Nk <= 0 || keep_window <= 0) return FDMA_ERR_INVALID;
+  if (mask_kind != FDMA_MASK_DENSE && mask_kind != FDMA_MASK_DENSE_U8) return FDMA_ERR_INVALID;
+  if (Nk > kTopkMaxKeys || (Nk & 7) != 0) return FDMA_ERR_UNSUPPORTED;
+  for (int a = 0; a < 3; ++a) {
+    if (bias_stride[a] < 0) return FDMA_ERR_INVALID;
+    if ((bias_stride[a] & 7) != 0) return FDMA_ERR_UNSUPPORTED;
+    // written in place or to a buffer of the same layout: rows must not alias
+    if (bias_out != nullptr && bias_stride[a] == 0) return FDMA_ERR_INVALID;
+  }
+  if (bias_out != nullptr && bias_stride[2] < Nk) return FDMA_ERR_INVALID;
+  if (!aligned16(bias) || !aligned16(mask) || (bias_out != nullptr && !aligned16(bias_out)))
+    return FDMA_ERR_UNSUPPORTED;
+  TopkParams p{};
+  p.B = B;
+  p.Hkv = Hkv;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.keep = keep_window;
+  for (int a = 0; a < 3; ++a) p.bias_stride[a] = bias_stride[a];
+  p.bias = static_cast<const uint16_t*>(bias);
+  p.bias_out = static_cast<uint16_t*>(bias_out);
+  if (mask_kind == FDMA_MASK_DENSE) p.mask_bf16 = static_cast<uint16_t*>(mask);
+  else p.mask_u8 = static_cast<uint8_t*>(mask);
+  return launch_topk(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FDMA_OK : FDMA_ERR_CUDA;
+}
+
 }  // extern "C"

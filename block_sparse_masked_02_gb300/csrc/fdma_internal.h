@@ -13,6 +13,7 @@ namespace fdma {
 
 constexpr int kTile = 128;           // query rows and key columns per tile
 constexpr int kMaxKTiles = 1024;     // Nk <= 131072
+constexpr int kTopkMaxKeys = 65536;  // one row's keys held in shared memory
 constexpr int kSkip = 0, kPartial = 1, kFull = 2;
 
 // Device error word values (first writer wins).
@@ -88,7 +89,18 @@ struct WorkspaceLayout {
 
 WorkspaceLayout workspace_layout(int B, int Nq, int Nk, int Hq, int Hkv, int d);
 
+struct TopkParams {
+  int B, Hkv, Nq, Nk, keep;
+  int64_t bias_stride[3];  // elements: batch, kv head, row (the key dimension is contiguous)
+  const uint16_t* bias;    // bf16
+  uint16_t* bias_out;      // bf16 with bias_stride, or nullptr; may equal bias
+  uint16_t* mask_bf16;     // (B,Hkv,Nq,Nk) contiguous, or nullptr
+  uint8_t* mask_u8;        // (B,Hkv,Nq,Nk) contiguous, or nullptr
+};
+
 cudaError_t launch_classify(const ClassifyParams& p, cudaStream_t stream);
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
+size_t topk_smem_bytes(int Nk);
 cudaError_t launch_fwd(int d, bool has_bias, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tb, const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream);

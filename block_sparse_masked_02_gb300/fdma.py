@@ -34,7 +34,7 @@ FDMA_FLAG_NO_SKIP = 2
 TILE = 128
 
 EXPORTED = ("fdma_workspace_size", "fdma_classify_blocks", "fdma_fwd", "fdma_bwd", "fdma_get_device_error",
-            "fdma_status_string", "fdma_fwd_noalloc")
+            "fdma_status_string", "fdma_fwd_noalloc", "fdma_topk_mask")
 
 
 class FdmaArgs(ctypes.Structure):
@@ -92,6 +92,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.fdma_status_string.restype = ctypes.c_char_p
     lib.fdma_fwd_noalloc.argtypes = [P, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     lib.fdma_fwd_noalloc.restype = ctypes.c_int
+    lib.fdma_topk_mask.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64)] + [ctypes.c_int] * 6 + \
+        [ctypes.c_void_p] * 3
+    lib.fdma_topk_mask.restype = ctypes.c_int
     _LIB = lib
     return lib
 
@@ -197,6 +200,37 @@ def classify_blocks(q, k, v, *, mask=None, colranges=None, causal=False, workspa
     _raise(load().fdma_classify_blocks(ctypes.byref(args), TILE, TILE, bm.data_ptr(), _stream_ptr(stream)),
            "fdma_classify_blocks")
     return bm
+
+
+def topk_mask(bias, keep_window, *, mask_dtype=torch.bfloat16, fill_bias=True, inplace=False, mask=None,
+              stream=None):
+    """Dynamic top-k mask of a bf16 bias (B, Hkv, Nq, Nk): returns (mask, bias_out).
+
+    mask is 1 at the keep_window largest bias entries of each row (ties: smaller key
+    index; selected entries equal to the bf16 minimum are not kept), 0 elsewhere, all
+    ones when Nk <= keep_window; dtype bf16 or uint8.  bias_out is the bias with the
+    bf16 minimum where the mask is 0 (the bias itself when inplace, a new tensor of the
+    same strides otherwise, None without fill_bias)."""
+    _check_cuda(bias, mask)
+    if bias.dtype != torch.bfloat16 or bias.dim() != 4 or bias.stride(3) != 1:
+        raise ValueError("bias must be bf16 (B, Hkv, Nq, Nk) with a contiguous last dimension")
+    if mask_dtype not in (torch.bfloat16, torch.uint8):
+        raise ValueError("mask_dtype must be torch.bfloat16 or torch.uint8")
+    B, Hkv, Nq, Nk = bias.shape
+    if mask is None:
+        mask = torch.empty((B, Hkv, Nq, Nk), dtype=mask_dtype, device=bias.device)
+    elif mask.dtype != mask_dtype or tuple(mask.shape) != (B, Hkv, Nq, Nk) or not mask.is_contiguous():
+        raise ValueError("mask must be a contiguous (B, Hkv, Nq, Nk) tensor of mask_dtype")
+    bias_out = None
+    if fill_bias:
+        bias_out = bias if inplace else torch.empty_strided(bias.shape, bias.stride(), dtype=bias.dtype,
+                                                             device=bias.device)
+    strides = (ctypes.c_int64 * 3)(*bias.stride()[:3])
+    kind = FDMA_MASK_DENSE if mask_dtype == torch.bfloat16 else FDMA_MASK_DENSE_U8
+    _raise(load().fdma_topk_mask(bias.data_ptr(), strides, B, Hkv, Nq, Nk, int(keep_window), kind, mask.data_ptr(),
+                                 bias_out.data_ptr() if bias_out is not None else None, _stream_ptr(stream)),
+           "fdma_topk_mask")
+    return mask, bias_out
 
 
 def fwd(q, k, v, *, mask=None, colranges=None, bias=None, causal=False, scale=None, workspace=None, flags=0,

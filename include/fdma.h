@@ -168,6 +168,23 @@ FDMA_API int fdma_bwd(const fdma_args* args, const void* out, const void* dout, 
    on one stream or synchronize between them. */
 FDMA_API int fdma_fwd_noalloc(const fdma_args* args, void* out, float* lse, void* stream);
 
+/* Dynamic top-k mask (Flash-DMA README, "Quick Start" example: the sparse mask built from
+   the bias before the attention call).  For every row (b, g, i) of bias, bf16 (B,Hkv,Nq,Nk):
+     - if Nk <= keep_window: every key is kept;
+     - else the keep_window keys of largest bias value are selected (equal values: the
+       smaller key index first; +0 and -0 are equal), and a selected key is kept unless its
+       bias equals the bf16 minimum (-3.3895e38).
+   mask: (B,Hkv,Nq,Nk) contiguous, 1 where kept and 0 elsewhere, bf16 (mask_kind =
+   FDMA_MASK_DENSE) or uint8 (FDMA_MASK_DENSE_U8).  bias_out (NULL: not written) receives the
+   bias where kept and the bf16 minimum elsewhere, laid out with bias_stride (so bias_out ==
+   bias rewrites the bias in place); with bias_out the strides must be nonzero and rows must
+   not overlap.  bias_stride: elements between batches, kv heads and rows (keys contiguous;
+   stride 0 broadcasts when bias_out is NULL).  Requirements: keep_window >= 1; Nk <= 65536
+   and a multiple of 8, strides multiples of 8 and pointers 16-byte aligned, else
+   FDMA_ERR_UNSUPPORTED.  Deterministic: the result does not depend on the launch. */
+FDMA_API int fdma_topk_mask(const void* bias, const int64_t bias_stride[3], int B, int Hkv, int Nq, int Nk,
+                            int keep_window, int mask_kind, void* mask, void* bias_out, void* stream);
+
 /* Synchronizes `stream`, returns the first kernel-side error recorded since the last call
    (FDMA_OK if none) and clears it. */
 FDMA_API int fdma_get_device_error(void* stream);

@@ -31,7 +31,8 @@ def F():
 
 def test_header_declares_the_entry_points():
     assert _declared() == sorted(["fdma_workspace_size", "fdma_classify_blocks", "fdma_fwd", "fdma_bwd",
-                                  "fdma_get_device_error", "fdma_status_string", "fdma_fwd_noalloc"])
+                                  "fdma_get_device_error", "fdma_status_string", "fdma_fwd_noalloc",
+                                  "fdma_topk_mask"])
 
 
 def test_library_exports_every_declared_symbol(F):
@@ -89,3 +90,18 @@ def test_missing_workspace_is_reported(F):
     lib = F.load()
     assert lib.fdma_fwd(ctypes.byref(a), 1 << 20, 1 << 20, None) == F.FDMA_ERR_WORKSPACE
     assert lib.fdma_classify_blocks(ctypes.byref(a), 128, 128, None, None) == F.FDMA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("Nk,keep,kind,stride_row,status", [
+    (64, 0, 1, 64, 1),        # keep_window must be >= 1
+    (60, 8, 1, 64, 2),        # Nk not a multiple of 8
+    (65544, 8, 1, 65544, 2),  # row longer than one CTA's shared memory
+    (64, 8, 2, 64, 1),        # mask kind must be dense bf16 or uint8
+    (64, 8, 1, 12, 2),        # row stride not a multiple of 8
+    (64, 8, 1, 56, 1),        # rows overlap while the bias is rewritten
+])
+def test_topk_argument_validation_before_any_cuda_call(F, Nk, keep, kind, stride_row, status):
+    lib = F.load()
+    strides = (ctypes.c_int64 * 3)(4 * stride_row, 2 * stride_row, stride_row)
+    rc = lib.fdma_topk_mask(1 << 20, strides, 1, 2, 2, Nk, keep, kind, 1 << 21, 1 << 20, None)
+    assert rc == status
