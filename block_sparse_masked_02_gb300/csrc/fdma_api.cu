@@ -71,6 +71,11 @@ int validate(const fdma_args* a, bool need_workspace) {
       for (int i = 0; i < 3; ++i)  // rows are read in pieces of 8 elements
         if (a->mask_stride[i] < 0 || a->mask_stride[i] % 8 != 0) return FDMA_ERR_UNSUPPORTED;
       break;
+    case FDMA_MASK_BITS:
+      if (a->mask == nullptr) return FDMA_ERR_INVALID;
+      for (int i = 0; i < 3; ++i)
+        if (a->mask_stride[i] < 0) return FDMA_ERR_INVALID;
+      break;
     case FDMA_MASK_COLRANGES:
     case FDMA_MASK_COLRANGES2:
       if (a->colranges == nullptr) return FDMA_ERR_INVALID;

@@ -11,8 +11,8 @@
 //     column-major (backward: one thread per key reads 16 bytes; bit r%32 of
 //     word r/32).  Bits outside the sequence are zero.
 //
-// Dense masks: one CTA per tile reads the tile once with 16-byte streaming
-// loads; each thread owns an 8x8 block, so the column-major copy is one 8x8
+// Dense masks (bf16, uint8 or bit-packed): one CTA per tile reads the tile once
+// (16-byte streaming loads for bf16); each thread owns an 8x8 block, so the column-major copy is one 8x8
 // bit transpose per thread.  Column ranges (and no mask): one warp per key tile
 // walks a run of query tiles; skip/full follow from per-column masked-row
 // counts, and keep bits are built a 32-row word at a time from the ranges.
@@ -87,7 +87,8 @@ __device__ __forceinline__ bool needs_bits(int kcls, bool ragged) {
 
 }  // namespace
 
-template <bool U8>
+// KIND: 0 = bf16 mask, 1 = uint8 / bool mask, 2 = bit-packed mask (one byte per 8 keys).
+template <int KIND>
 __global__ void __launch_bounds__(256) classify_dense_kernel(const ClassifyParams p) {
   __shared__ __align__(16) uint8_t rowbits[kTile][16];  // bit (c & 7) of byte c >> 3 = keep(q0 + r, k0 + c)
   __shared__ __align__(16) uint8_t colbits[kTile][16];  // bit (r & 7) of byte r >> 3
@@ -113,10 +114,17 @@ __global__ void __launch_bounds__(256) classify_dense_kernel(const ClassifyParam
   // Thread -> 8x8 block: rows rb*8 .. rb*8+7, columns cc*8 .. cc*8+7.  For each
   // row step a warp reads two whole 256-byte row segments.
   const int cc = tid & 15, rb = tid >> 4;
-  const int64_t off = b * p.ms_b + g * p.ms_h + static_cast<int64_t>(q0 + rb * 8) * p.ms_r + k0 + cc * 8;
+  const int64_t row_off = b * p.ms_b + g * p.ms_h + static_cast<int64_t>(q0 + rb * 8) * p.ms_r;
+  const int64_t off = row_off + k0 + cc * 8;
   const int ncol = cols - cc * 8;  // valid columns of this thread's chunk
   uint64_t blk = 0;                // bit 8u+e = keep(row rb*8+u, column cc*8+e)
-  if (U8) {
+  if (KIND == 2) {
+    // the mask byte of columns cc*8 .. cc*8+7 is already this block row's keep bits
+    const uint8_t* base = p.mask_u8 + row_off + ((k0 + cc * 8) >> 3);
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (rb * 8 + u < rows && ncol > 0) blk |= static_cast<uint64_t>(base[u * p.ms_r]) << (8 * u);
+  } else if (KIND == 1) {
     const uint8_t* base = p.mask_u8 + off;
     uint2 raw[8];
 #pragma unroll
@@ -312,12 +320,14 @@ __global__ void __launch_bounds__(256) classify_ranges_kernel(const ClassifyPara
 }
 
 cudaError_t launch_classify(const ClassifyParams& p, cudaStream_t stream) {
-  if (p.mask_kind == FDMA_MASK_DENSE || p.mask_kind == FDMA_MASK_DENSE_U8) {
+  if (p.mask_kind == FDMA_MASK_DENSE || p.mask_kind == FDMA_MASK_DENSE_U8 || p.mask_kind == FDMA_MASK_BITS) {
     dim3 grid(p.nTk, p.nTq, p.B * p.Hkv);
     if (p.mask_kind == FDMA_MASK_DENSE_U8)
-      classify_dense_kernel<true><<<grid, 256, 0, stream>>>(p);
+      classify_dense_kernel<1><<<grid, 256, 0, stream>>>(p);
+    else if (p.mask_kind == FDMA_MASK_BITS)
+      classify_dense_kernel<2><<<grid, 256, 0, stream>>>(p);
     else
-      classify_dense_kernel<false><<<grid, 256, 0, stream>>>(p);
+      classify_dense_kernel<0><<<grid, 256, 0, stream>>>(p);
   } else {
     const int64_t warps = static_cast<int64_t>(p.B) * p.Hkv * p.nTk * ((p.nTq + kRangeChunk - 1) / kRangeChunk);
     classify_ranges_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(p);

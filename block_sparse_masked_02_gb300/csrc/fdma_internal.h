@@ -28,7 +28,7 @@ struct ClassifyParams {
   int mask_kind, causal, no_skip;
   int causal_off;  // Nk - Nq: key j is visible from query i when j <= i + causal_off
   const uint16_t* mask;
-  const uint8_t* mask_u8;  // same buffer, FDMA_MASK_DENSE_U8
+  const uint8_t* mask_u8;  // same buffer, FDMA_MASK_DENSE_U8 / FDMA_MASK_BITS
   int64_t ms_b, ms_h, ms_r;
   const int32_t* cr;
   int64_t cr_b, cr_h;

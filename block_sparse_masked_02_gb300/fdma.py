@@ -27,6 +27,7 @@ FDMA_MASK_DENSE = 1
 FDMA_MASK_COLRANGES = 2
 FDMA_MASK_DENSE_U8 = 3
 FDMA_MASK_COLRANGES2 = 4
+FDMA_MASK_BITS = 5
 
 FDMA_FLAG_REUSE_CLASSIFICATION = 1
 FDMA_FLAG_NO_SKIP = 2
@@ -118,6 +119,31 @@ def _stream_ptr(stream) -> int:
     return s.cuda_stream
 
 
+class PackedMask:
+    """A bit-packed keep mask: uint8 (B, Hkv, Nq, ceil(Nk/8)), key j of a row is bit j & 7 of
+    byte j >> 3 (least significant bit first), with a contiguous last dimension.  Pass it as
+    `mask=` to classify_blocks / fwd / bwd."""
+
+    def __init__(self, bits: torch.Tensor, nk: int):
+        if bits.dtype != torch.uint8 or bits.dim() != 4 or bits.stride(3) != 1:
+            raise ValueError("packed mask must be uint8 (B, Hkv, Nq, ceil(Nk/8)) with a contiguous last dim")
+        if bits.shape[3] != -(-nk // 8):
+            raise ValueError("packed mask has ceil(Nk/8) bytes per row")
+        self.bits, self.nk = bits, int(nk)
+        self.is_cuda = bits.is_cuda
+
+
+def pack_mask(mask: torch.Tensor) -> PackedMask:
+    """Bit-pack a (B, Hkv, Nq, Nk) mask (nonzero = keep) on its device."""
+    B, H, Nq, Nk = mask.shape
+    nb = -(-Nk // 8)
+    keep = torch.zeros((B, H, Nq, nb * 8), dtype=torch.uint8, device=mask.device)
+    keep[..., :Nk] = (mask != 0).to(torch.uint8)
+    weights = (1 << torch.arange(8, device=mask.device, dtype=torch.int32)).to(torch.uint8)
+    bits = (keep.view(B, H, Nq, nb, 8) * weights).sum(dim=-1, dtype=torch.int32).to(torch.uint8)
+    return PackedMask(bits.contiguous(), Nk)
+
+
 def make_args(q, k, v, *, mask=None, colranges=None, bias=None, causal=False, scale=None, workspace=None,
               flags=0) -> FdmaArgs:
     """Fill fdma_args from tensors: q (B,Nq,Hq,d), k/v (B,Nk,Hkv,d) with a contiguous
@@ -134,7 +160,13 @@ def make_args(q, k, v, *, mask=None, colranges=None, bias=None, causal=False, sc
         getattr(a, name + "_stride")[:] = [t.stride(0), t.stride(1), t.stride(2)]
     if mask is not None and colranges is not None:
         raise ValueError("pass either mask or colranges")
-    if mask is not None:
+    if isinstance(mask, PackedMask):
+        if mask.nk != a.Nk:
+            raise ValueError("packed mask was built for another key length")
+        a.mask_kind = FDMA_MASK_BITS
+        a.mask = mask.bits.data_ptr()
+        a.mask_stride[:] = [mask.bits.stride(0), mask.bits.stride(1), mask.bits.stride(2)]
+    elif mask is not None:
         if mask.dtype not in (torch.bfloat16, torch.uint8, torch.bool) or mask.stride(3) != 1:
             raise ValueError("mask must be bf16, uint8 or bool with contiguous columns")
         a.mask_kind = FDMA_MASK_DENSE if mask.dtype == torch.bfloat16 else FDMA_MASK_DENSE_U8

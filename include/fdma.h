@@ -70,7 +70,8 @@ typedef enum {
   FDMA_MASK_DENSE = 1,       /* bf16 (B,Hkv,Nq,Nk), nonzero = keep */
   FDMA_MASK_COLRANGES = 2,   /* int32 (B,Hkv,Nk,2): one masked query-row range per key column */
   FDMA_MASK_DENSE_U8 = 3,    /* uint8 / bool (B,Hkv,Nq,Nk), nonzero = keep */
-  FDMA_MASK_COLRANGES2 = 4   /* int32 (B,Hkv,Nk,4): two masked query-row ranges per key column */
+  FDMA_MASK_COLRANGES2 = 4,  /* int32 (B,Hkv,Nk,4): two masked query-row ranges per key column */
+  FDMA_MASK_BITS = 5         /* uint8 (B,Hkv,Nq,ceil(Nk/8)) bit-packed: bit (j & 7) of byte j >> 3 = keep */
 } fdma_mask_kind;
 
 /* flags */
@@ -95,7 +96,10 @@ typedef struct fdma_args {
   /* FDMA_MASK_DENSE: bf16 (B,Hkv,Nq,Nk), nonzero = keep (both signed zeros count as zero).
      FDMA_MASK_DENSE_U8: uint8 (or bool) (B,Hkv,Nq,Nk), nonzero = keep.
      Strides (batch, head, row) in elements, columns contiguous; every stride a multiple of 8
-     elements (0 broadcasts a batch or head), base 16-byte aligned (else FDMA_ERR_UNSUPPORTED). */
+     elements (0 broadcasts a batch or head), base 16-byte aligned (else FDMA_ERR_UNSUPPORTED).
+     FDMA_MASK_BITS: uint8 (B,Hkv,Nq,ceil(Nk/8)), one bit per key, least significant bit first
+     (key j of row i is bit j & 7 of byte j >> 3); bits past Nk are ignored.  Strides (batch,
+     head, row) in bytes, any alignment (0 broadcasts a batch or head). */
   const void* mask;
   int64_t mask_stride[3];
   /* FDMA_MASK_COLRANGES: int32 (B,Hkv,Nk,2): query rows [start,end) are MASKED for key

@@ -11,7 +11,8 @@ Definition followed (Flash-DMA README, "Quick Start" example and
 "Key Features"; Flash-DMA issue #73, "Project Progress"; FlashMask README,
 "Formulation"):
 
-    keep(b,g,i,j) = mask[b,g,i,j] != 0            (dense 4D mask, per kv head; bf16, uint8 or bool)
+    keep(b,g,i,j) = mask[b,g,i,j] != 0            (dense 4D mask, per kv head; bf16, uint8 or bool;
+                                                   or bit-packed: bit j % 8 of byte j // 8 of row i)
                   | not (start[b,g,j] <= i < end[b,g,j])   (column ranges: one masked
                                                             row range per key column,
                                                             or two, masked as a union)
@@ -71,13 +72,16 @@ class Problem:
     """Inputs of one attention call, as given to both implementations.
 
     q (B,Nq,Hq,d), k/v (B,Nk,Hkv,d), dout like q; bias and mask (B,Hkv,Nq,Nk)
-    or None; colranges (B,Hkv,Nk,2) or (B,Hkv,Nk,4) int or None.  Tensors may be torch (any
-    dtype, any device) or numpy; slices are converted to float64 on demand.
+    or None; colranges (B,Hkv,Nk,2) or (B,Hkv,Nk,4) int or None; mask_bits: the mask
+    bit-packed, uint8 (B,Hkv,Nq,ceil(Nk/8)), key j of a row = bit j % 8 of byte j // 8.
+    Tensors may be torch (any dtype, any device) or numpy; slices are converted to float64
+    on demand.
     """
 
-    def __init__(self, q, k, v, *, bias=None, mask=None, colranges=None, causal=False, scale=None, dout=None):
+    def __init__(self, q, k, v, *, bias=None, mask=None, colranges=None, causal=False, scale=None, dout=None,
+                 mask_bits=None):
         self.q, self.k, self.v = q, k, v
-        self.bias, self.mask, self.colranges = bias, mask, colranges
+        self.bias, self.mask, self.colranges, self.mask_bits = bias, mask, colranges, mask_bits
         self.causal = bool(causal)
         self.B, self.Nq, self.Hq, self.d = (int(s) for s in q.shape)
         self.Nk, self.Hkv = int(k.shape[1]), int(k.shape[2])
@@ -85,8 +89,8 @@ class Problem:
         self.G = self.Hq // self.Hkv
         self.scale = 1.0 / math.sqrt(self.d) if scale is None else float(scale)
         self.dout = dout
-        if mask is not None and colranges is not None:
-            raise ValueError("give a dense mask or column ranges, not both")
+        if sum(x is not None for x in (mask, colranges, mask_bits)) > 1:
+            raise ValueError("give one of a dense mask, a bit-packed mask or column ranges")
 
 
 def keep_rows(p: Problem, b: int, g: int, r0: int, r1: int) -> np.ndarray:
@@ -95,6 +99,10 @@ def keep_rows(p: Problem, b: int, g: int, r0: int, r1: int) -> np.ndarray:
     j = np.arange(p.Nk)[None, :]
     if p.mask is not None:
         keep = _f64(p.mask[b, g, r0:r1, :]) != 0.0
+    elif p.mask_bits is not None:
+        raw = _i64(p.mask_bits[b, g, r0:r1, :])  # (R, ceil(Nk/8)) byte values
+        bit = (raw[:, :, None] >> np.arange(8)[None, None, :]) & 1  # bit e of byte c = key 8c+e
+        keep = bit.reshape(r1 - r0, -1)[:, :p.Nk] != 0
     elif p.colranges is not None:
         cr = _i64(p.colranges[b, g])  # (Nk, 2) or (Nk, 4)
         masked = (cr[:, 0][None, :] <= i) & (i < cr[:, 1][None, :])

@@ -321,3 +321,49 @@ def test_argument_errors(F):
     with pytest.raises(F.FdmaError) as e:
         F.fwd(q, k, k, mask=m132, causal=True)
     assert e.value.status == F.FDMA_ERR_UNSUPPORTED
+
+
+def test_bit_packed_mask(F):
+    """A bit-packed mask (uint8, least significant bit first) gives the same tiles and
+    bit-identical results as the bf16 mask it was packed from, also through a padded row
+    stride, and matches the oracle for a key length that is not a multiple of 8."""
+    wl = W.scaled(W.WORKLOADS["n4096_hq32_hkv8"], Nq=392, Nk=264, Hq=4, Hkv=2, keep_window=96, seed=31)
+    inp = W.make_inputs(wl)
+    q, k, v, bias, do = (inp[n].cuda() for n in ("q", "k", "v", "bias", "dout"))
+    dense = inp["mask"].cuda()
+    packed = np.packbits((inp["mask"] != 0).numpy(), axis=-1, bitorder="little")
+    buf = torch.zeros((*packed.shape[:3], 48), dtype=torch.uint8)
+    buf[..., :packed.shape[3]] = torch.from_numpy(packed)
+    pm = F.PackedMask(buf.cuda()[..., :packed.shape[3]], wl.Nk)  # row stride 48 bytes
+    assert torch.equal(F.classify_blocks(q, k, v, mask=dense, causal=True),
+                       F.classify_blocks(q, k, v, mask=pm, causal=True))
+    a = F.fwd(q, k, v, mask=dense, bias=bias, causal=True, scale=wl.scale)
+    b = F.fwd(q, k, v, mask=pm, bias=bias, causal=True, scale=wl.scale)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    ga = F.bwd(q, k, v, a[0], do, a[1], mask=dense, bias=bias, causal=True, scale=wl.scale)
+    gb = F.bwd(q, k, v, b[0], do, b[1], mask=pm, bias=bias, causal=True, scale=wl.scale)
+    for x, y in zip(ga, gb):
+        assert torch.equal(x, y)
+    assert F.device_error() == 0
+    # key length 203 (not a multiple of 8), no bias: against the oracle
+    g = torch.Generator().manual_seed(37)
+    B, Nq, Nk, Hq, Hkv, d = 1, 300, 203, 4, 2, 64
+    t = dict(q=torch.randn(B, Nq, Hq, d, generator=g).bfloat16(), k=torch.randn(B, Nk, Hkv, d, generator=g).bfloat16(),
+             v=torch.randn(B, Nk, Hkv, d, generator=g).bfloat16(), dout=torch.randn(B, Nq, Hq, d, generator=g).bfloat16())
+    keep = torch.rand(B, Hkv, Nq, Nk, generator=g) < 0.3
+    bits = torch.from_numpy(np.packbits(keep.numpy(), axis=-1, bitorder="little"))
+    qc, kc, vc, dc = (t[n].cuda() for n in ("q", "k", "v", "dout"))
+    pmc = F.PackedMask(bits.cuda(), Nk)
+    out, lse = F.fwd(qc, kc, vc, mask=pmc, causal=True, scale=0.125)
+    dq, dk, dv, _ = F.bwd(qc, kc, vc, out, dc, lse, mask=pmc, causal=True, scale=0.125, want_dbias=False)
+    assert F.device_error() == 0
+    p = orc.Problem(t["q"], t["k"], t["v"], mask_bits=bits, causal=True, scale=0.125, dout=t["dout"])
+    O, L = orc.forward(p)
+    o_gpu = out.float().cpu().numpy()
+    assert np.abs(o_gpu - O).max() <= O_MAXABS and rel_l2(o_gpu, O) <= O_RELL2
+    fin = ~np.isneginf(L)
+    assert np.array_equal(np.isneginf(lse.cpu().numpy()), ~fin)
+    assert np.abs(lse.cpu().numpy()[fin] - L[fin]).max(initial=0.0) <= LSE_ABS
+    rq, rk, rv, _ = orc.backward(p, want_dbias=False)
+    for name, x, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        assert rel_l2(x.float().cpu().numpy(), ref) <= G_RELL2, name

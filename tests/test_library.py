@@ -105,3 +105,14 @@ def test_topk_argument_validation_before_any_cuda_call(F, Nk, keep, kind, stride
     strides = (ctypes.c_int64 * 3)(4 * stride_row, 2 * stride_row, stride_row)
     rc = lib.fdma_topk_mask(1 << 20, strides, 1, 2, 2, Nk, keep, kind, 1 << 21, 1 << 20, None)
     assert rc == status
+
+
+def test_pack_mask_matches_numpy_packbits(F):
+    import numpy as np
+    import torch
+    g = torch.Generator().manual_seed(4)
+    for nk in (16, 21, 130):
+        m = (torch.rand(2, 3, 5, nk, generator=g) < 0.4).to(torch.bfloat16)
+        pm = F.pack_mask(m)
+        ref = np.packbits((m != 0).numpy(), axis=-1, bitorder="little")
+        assert pm.nk == nk and np.array_equal(pm.bits.numpy(), ref)

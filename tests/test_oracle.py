@@ -397,3 +397,15 @@ def test_effective_flops_counts_active_tiles():
     bm = np.array([[[[2, 0], [1, 2]]]], dtype=np.int8)
     f = orc.effective_flops(bm, Hq=4, Hkv=1, d=128)
     assert f["fwd"] == 4 * 128 * 128 * 128 * 3 * 4 and f["bwd"] == 10 * 128 * 128 * 128 * 3 * 4
+
+
+def test_bit_packed_mask_equals_the_dense_mask():
+    # bits packed by numpy (least significant bit first) give the same keep set, also for
+    # a key length that is not a multiple of 8
+    for nk in (33, 40):
+        p = _problem(41, B=1, Nq=29, Nk=nk, Hq=2, Hkv=1, d=4, causal=True, mask="dense", density=0.5)
+        packed = np.packbits((p.mask != 0).numpy(), axis=-1, bitorder="little")
+        alt = orc.Problem(p.q, p.k, p.v, bias=p.bias, mask_bits=packed, causal=True, scale=p.scale, dout=p.dout)
+        assert np.array_equal(orc.keep_rows(alt, 0, 0, 0, 29), orc.keep_rows(p, 0, 0, 0, 29))
+        o, ref = orc.forward(alt), orc.forward(p)
+        assert np.array_equal(o[0], ref[0]) and np.array_equal(o[1], ref[1])
