@@ -135,7 +135,9 @@ struct BwdSmem {
   static constexpr uint32_t kOffDelta = kOffLse + 1024;  // [2][128] f32
   static constexpr uint32_t kOffBar = kOffDelta + 1024;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBwdBars * 8;
-  static constexpr uint32_t kTotal = kOffMisc + 16;
+  static constexpr uint32_t kOffMap = kOffMisc + 16;  // this key tile's column of the block map, 2 bits per query tile
+  static constexpr uint32_t kTotal = kOffMap + kMaxKTiles / 4;
+  static_assert(kTotal <= 232448, "bwd shared memory exceeds the per-CTA limit");
 };
 
 __device__ __forceinline__ uint64_t kmajor_step(int k, uint32_t rows) {
@@ -143,14 +145,16 @@ __device__ __forceinline__ uint64_t kmajor_step(int k, uint32_t rows) {
 }
 __device__ __forceinline__ uint64_t mnmajor_step(int k) { return static_cast<uint64_t>((k * 2048) >> 4); }
 
-// Iterates the active query tiles of one key-tile column of the block map.
+// The active query tiles of one key-tile column of the block map, from a shared-memory
+// copy packed 2 bits per query tile (kSkip / kPartial / kFull).
 struct ColIter {
-  const int8_t* col;  // &kmap[(b*Hkv+g)*nTq*nTk + kt]
-  int nTk, nTq;
+  const uint8_t* map2;
+  int nTq;
+  __device__ __forceinline__ int cls(int qt) const { return (map2[qt >> 2] >> ((qt & 3) * 2)) & 3; }
   __device__ __forceinline__ int next(int qt) const {
     do {
       ++qt;
-    } while (qt < nTq && col[static_cast<int64_t>(qt) * nTk] == kSkip);
+    } while (qt < nTq && cls(qt) == kSkip);
     return qt;
   }
 };
@@ -196,7 +200,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int kt = id / p.B;  // small key tiles (most causal work) first
   const int k0 = kt * kTile;
   const int64_t col_base = static_cast<int64_t>(b * p.Hkv + g) * p.nTq * p.nTk + kt;
-  const ColIter it{p.kmap + col_base, p.nTk, p.nTq};
+  uint8_t* map2 = smem + L::kOffMap;
+  const ColIter it{map2, p.nTq};
   const bool ragged_k = (p.Nk & (kTile - 1)) != 0 && kt == p.nTk - 1;
   const bool ragged_q_any = (p.Nq & (kTile - 1)) != 0;
 
@@ -211,6 +216,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bars[kBEmpty], 256);
     misc[1] = 0;
     fence_mbar_init();
+  }
+  for (int q = threadIdx.x; q < (p.nTq + 3) / 4; q += blockDim.x) {
+    uint32_t v = 0;
+    for (int e = 0; e < 4; ++e) {
+      const int qt = 4 * q + e;
+      if (qt < p.nTq) v |= static_cast<uint32_t>(p.kmap[col_base + static_cast<int64_t>(qt) * p.nTk] & 3) << (2 * e);
+    }
+    map2[q] = static_cast<uint8_t>(v);
   }
   if (warp == 1) {
     tmem_alloc(misc, 512);
@@ -370,10 +383,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // barrier below; after a failed wait (ok == false) the work and the stores are skipped.
     for (int qt = first_qt; qt < p.nTq; qt = it.next(qt), ++qi_count) {
       const int q0 = qt * kTile;
-      const int64_t tile = col_base + static_cast<int64_t>(qt) * p.nTk;
-      const bool partial = p.kmap[tile] == kPartial || ragged_k || (ragged_q_any && qt == p.nTq - 1);
+      const bool partial = it.cls(qt) == kPartial || ragged_k || (ragged_q_any && qt == p.nTq - 1);
       uint32_t bw0 = ~0u, bw1 = ~0u;  // keep bits of queries qbase..qbase+63 for key j
       if (partial) {
+        const int64_t tile = col_base + static_cast<int64_t>(qt) * p.nTk;
         const uint2 bb = reinterpret_cast<const uint2*>(&p.bits_col[tile * kTile + j])[wg];
         bw0 = bb.x;
         bw1 = bb.y;
@@ -523,7 +536,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ctid == 0 && ok) {
         const uint64_t zpol = l2_evict_first();
         for (int qt = 0; qt < p.nTq; ++qt) {
-          if (p.kmap[col_base + static_cast<int64_t>(qt) * p.nTk] != kSkip) continue;
+          if (it.cls(qt) != kSkip) continue;
           tma_store_4d_hint(&tmDB, sDS, k0, qt * kTile, g, b, zpol);
           tma_store_4d_hint(&tmDB, sDS + 16384, k0 + 64, qt * kTile, g, b, zpol);
         }
