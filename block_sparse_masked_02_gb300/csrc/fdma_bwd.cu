@@ -381,21 +381,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     // No compute thread leaves these loops early, so every one of them reaches every named
     // barrier below; after a failed wait (ok == false) the work and the stores are skipped.
-    for (int qt = first_qt; qt < p.nTq; qt = it.next(qt), ++qi_count) {
-      const int q0 = qt * kTile;
+    // Per query tile: the keep bits of queries qbase..qbase+63 for key j and the bias^T column
+    // slice, copied once into registers for every head.  The next tile's are fetched while
+    // the last head of the current tile waits for its dQ product.
+    uint32_t bw0 = ~0u, bw1 = ~0u;
+    uint32_t bpk[HAS_BIAS ? 32 : 1];
+    auto fetch_tile = [&](int qt, int qi) {
       const bool partial = it.cls(qt) == kPartial || ragged_k || (ragged_q_any && qt == p.nTq - 1);
-      uint32_t bw0 = ~0u, bw1 = ~0u;  // keep bits of queries qbase..qbase+63 for key j
+      bw0 = ~0u;
+      bw1 = ~0u;
       if (partial) {
         const int64_t tile = col_base + static_cast<int64_t>(qt) * p.nTk;
         const uint2 bb = reinterpret_cast<const uint2*>(&p.bits_col[tile * kTile + j])[wg];
         bw0 = bb.x;
         bw1 = bb.y;
       }
-      const int rows_in = min(kTile, p.Nq - q0) - qbase;  // valid queries in this half
-      // bias^T column slice of this query tile, copied once into registers for every head
-      uint32_t bpk[HAS_BIAS ? 32 : 1];
       if (HAS_BIAS) {
-        ok = ok && mbar_wait(&bars[kBFull], qi_count & 1, p.err, kDevErrTimeout, abort_flag);
+        ok = ok && mbar_wait(&bars[kBFull], qi & 1, p.err, kDevErrTimeout, abort_flag);
         const uint8_t* bt = sBias + (j >> 6) * 16384 + (j & 7) * 2;
         const int jc = (j & 63) >> 3;
 #pragma unroll
@@ -407,6 +409,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mbar_arrive(&bars[kBEmpty]);
       }
+    };
+    if (first_qt < p.nTq) fetch_tile(first_qt, 0);
+    for (int qt = first_qt; qt < p.nTq; qt = it.next(qt), ++qi_count) {
+      const int q0 = qt * kTile;
+      const int rows_in = min(kTile, p.Nq - q0) - qbase;  // valid queries in this half
       for (int hh = 0; hh < p.G; ++hh, ++n) {
         const int h = g * p.G + hh;
         const int s = n & 1;
@@ -465,6 +472,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars[kPReady]);
+        if (hh == p.G - 1) {  // the bits and bias^T slice of this tile are no longer needed
+          const int nq = it.next(qt);
+          if (nq < p.nTq) fetch_tile(nq, qi_count + 1);
+        }
         // drain dQ into the fp32 accumulator
         if (!(ok = mbar_wait(&bars[kDqFull], n & 1, p.err, kDevErrTimeout, abort_flag))) continue;
         tc_fence_after();
