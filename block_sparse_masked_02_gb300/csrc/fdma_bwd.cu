@@ -421,6 +421,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ok = ok && mbar_wait(&bars[kDpFull], n & 1, p.err, kDevErrTimeout, abort_flag);
         ok = ok && mbar_wait(&bars[kQFull + s], (n >> 1) & 1, p.err, kDevErrTimeout, abort_flag);
         ok = ok && (n == 0 || mbar_wait(&bars[kDsFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag));
+        if (WANT_DBIAS && hh == 0 && qi_count > 0) {
+          // the previous tile's dBias store must have read the dS^T tile before it is rewritten
+          if (ctid == 0) bulk_wait_read_all();
+          named_bar_sync(1, 256);
+        }
         if (!ok) continue;
         tc_fence_after();
         const float* lse2 = sLse + s * 128 + qbase;
@@ -531,14 +536,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_store_4d_hint(&tmDB, sDS, k0, q0, g, b, pol);
           tma_store_4d_hint(&tmDB, sDS + 16384, k0 + 64, q0, g, b, pol);
           bulk_commit_group();
-          bulk_wait_read_all();
         }
-        named_bar_sync(1, 256);
       }
     }
     if (ok && n > 0) ok = mbar_wait(&bars[kFinal], 0, p.err, kDevErrTimeout, abort_flag);
     // zero-fill the dBias tiles of this key column that were skipped (TMA stores of a zero tile)
     if (WANT_DBIAS) {
+      if (ctid == 0) bulk_wait_read_all();  // the last tile's dBias store has read the dS^T tile
+      named_bar_sync(1, 256);
       reinterpret_cast<uint4*>(sDS)[ctid * 8 + 0] = make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int u = 1; u < 8; ++u) reinterpret_cast<uint4*>(sDS)[ctid * 8 + u] = make_uint4(0, 0, 0, 0);
