@@ -36,7 +36,7 @@ KERNELS_PER_STEP = 5  # classify, fwd, bwd_pre, bwd, dq_convert
 # DRAM bytes (read + write) of one bwd_kernel launch on this workload: an ncu capture of
 # bwd_kernel on n4096_hq32_hkv8 (332.57 MB read + 306.41 MB written) scaled by the active
 # (tile, head) units, 132096 / 16896; None whenever the kernel has changed since that capture.
-BWD_TRAFFIC_BYTES = round((332.570368e6 + 306.414336e6) * 132096 / 16896)
+BWD_TRAFFIC_BYTES = None
 
 
 def _peaks():
