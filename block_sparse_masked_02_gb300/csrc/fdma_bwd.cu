@@ -405,7 +405,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const int i0 = qbase + 2 * e, i1 = i0 + 1;
           const uint32_t lo = *reinterpret_cast<const uint16_t*>(bt + i0 * 128 + ((jc ^ (i0 & 7)) << 4));
           const uint32_t hi = *reinterpret_cast<const uint16_t*>(bt + i1 * 128 + ((jc ^ (i1 & 7)) << 4));
-          bpk[e] = lo | (hi << 16);
+          // masked (query, key) pairs get a bias of -inf (bf16 0xFF80): their P is exp2(-inf) = 0
+          const uint32_t wd = e < 16 ? bw0 : bw1;
+          const bool k0b = (wd >> ((2 * e) & 31)) & 1u, k1b = (wd >> ((2 * e + 1) & 31)) & 1u;
+          bpk[e] = (k0b ? lo : 0xFF80u) | ((k1b ? hi : 0xFF80u) << 16);
         }
         mbar_arrive(&bars[kBEmpty]);
       }
@@ -455,8 +458,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                          : fma2(s2, sc2, nl[e >> 1]);
             float x0, x1;
             f2split(x2, x0, x1);
-            const float p0 = ((word >> (qi & 31)) & 1u) ? ex2(x0) : 0.f;
-            const float p1 = ((word >> ((qi + 1) & 31)) & 1u) ? ex2(x1) : 0.f;
+            // with a bias the keep bits are already folded into it as -inf
+            const float p0 = (HAS_BIAS || ((word >> (qi & 31)) & 1u)) ? ex2(x0) : 0.f;
+            const float p1 = (HAS_BIAS || ((word >> ((qi + 1) & 31)) & 1u)) ? ex2(x1) : 0.f;
             const uint64_t dv2 =
                 mul2(f2(p0, p1), sub2(f2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), dd[e >> 1]));
             if (WANT_DBIAS) acc2[qi >> 1] = add2(acc2[qi >> 1], dv2);
