@@ -163,6 +163,15 @@ __device__ __forceinline__ void red_add_f32(float* gptr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(gptr), "f"(v) : "memory");
 }
 
+// dO slot of step n (head hh of its query tile).  Without a bias there are two dO slots,
+// used alternately.  With a bias the second slot is the bias buffer (it directly follows the
+// dO slot): head hh uses it when G-1-hh is odd, so the last head of every query tile uses
+// slot 0 and the buffer is free to receive the next tile's bias during that head.
+template <bool HAS_BIAS>
+__device__ __forceinline__ int do_slot(int n, int hh, int G) {
+  return HAS_BIAS ? ((G - 1 - hh) & 1) : (n & 1);
+}
+
 template <int D, bool HAS_BIAS, bool WANT_DBIAS>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -171,7 +180,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                const BwdParams p) {
   using L = BwdSmem<D, HAS_BIAS>;
   constexpr int KB = D / 64;
-  constexpr int DOS = L::kDoStages;
   constexpr bool DQ_T = (D == 128);  // dQ^T = K^T dS^T (lane = head-dim index) for coalesced reductions
   constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);   // S^T, dP^T
   constexpr uint32_t IDESC_DV = idesc_bf16(128, D, false, true);     // P^T(tmem) x dO (N contiguous)
@@ -252,17 +260,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_load_4d(sK + c * 16384, &tmK, &bars[kKVFull], c * 64, k0, g, b);
       tma_load_4d(sV + c * 16384, &tmV, &bars[kKVFull], c * 64, k0, g, b);
     }
-    int n = 0, qi_count = 0;
+    int n = 0, qi_count = 0, nbias = 0;
+    int ufill0 = 0, ufill1 = 0;  // dO fills of slot 0 / slot 1
     bool ok = true;
-    for (int qt = first_qt; ok && qt < p.nTq; qt = it.next(qt), ++qi_count) {
-      if (HAS_BIAS) {
-        if (!(ok = mbar_wait(&bars[kBEmpty], (qi_count & 1) ^ 1, p.err, kDevErrTimeout, abort_flag))) break;
-        mbar_arrive_expect_tx(&bars[kBFull], 32768);
+    auto load_bias = [&](int qt) {
+      mbar_arrive_expect_tx(&bars[kBFull], 32768);
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-          tma_load_4d_hint(sBias + c * 16384, &tmB, &bars[kBFull], k0 + c * 64, qt * kTile, g * p.bias_hsel,
-                           b * p.bias_bsel, bias_pol);
-      }
+      for (int c = 0; c < 2; ++c)
+        tma_load_4d_hint(sBias + c * 16384, &tmB, &bars[kBFull], k0 + c * 64, qt * kTile, g * p.bias_hsel,
+                         b * p.bias_bsel, bias_pol);
+      ++nbias;
+    };
+    if (HAS_BIAS) load_bias(first_qt);  // the first bias tile has no predecessor in its buffer
+    for (int qt = first_qt; ok && qt < p.nTq; qt = it.next(qt), ++qi_count) {
       for (int hh = 0; hh < p.G; ++hh, ++n) {
         const int h = g * p.G + hh;
         const int s = n & 1;
@@ -274,22 +284,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int64_t vec = (static_cast<int64_t>(b) * p.Hq + h) * p.nqpad + qt * kTile;
         bulk_load(sLse + s * 128, p.lse2 + vec, 512, &bars[kQFull + s]);
         bulk_load(sDelta + s * 128, p.delta + vec, 512, &bars[kQFull + s]);
-        const int sd = n % DOS;
-        if (!(ok = mbar_wait(&bars[kDoEmpty + sd], ((n / DOS) & 1) ^ 1, p.err, kDevErrTimeout, abort_flag))) break;
+        const int sd = do_slot<HAS_BIAS>(n, hh, p.G);
+        const int u = sd ? ufill1 : ufill0;
+        if (HAS_BIAS && sd == 1 && hh == (((p.G - 1) & 1) ? 0 : 1)) {
+          // first use of the bias buffer in this tile: the tile's bias must have been copied out
+          if (!(ok = mbar_wait(&bars[kBEmpty], qi_count & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        } else {
+          if (!(ok = mbar_wait(&bars[kDoEmpty + sd], (u & 1) ^ 1, p.err, kDevErrTimeout, abort_flag))) break;
+        }
         mbar_arrive_expect_tx(&bars[kDoFull + sd], L::kQB);
 #pragma unroll
         for (int c = 0; c < KB; ++c)
           tma_load_4d(sDO + sd * L::kQB + c * 16384, &tmDO, &bars[kDoFull + sd], c * 64, qt * kTile, h, b);
+        if (sd) ufill1 = u + 1;
+        else ufill0 = u + 1;
+      }
+      if (!ok) break;
+      if (HAS_BIAS) {
+        const int nq = it.next(qt);
+        if (nq < p.nTq) {
+          // the next tile's bias goes into the buffer once its last dO there (or, with one head
+          // per group, this tile's bias) has been released
+          if (p.G >= 2) ok = mbar_wait(&bars[kDoEmpty + 1], (ufill1 - 1) & 1, p.err, kDevErrTimeout, abort_flag);
+          else ok = mbar_wait(&bars[kBEmpty], qi_count & 1, p.err, kDevErrTimeout, abort_flag);
+          if (!ok) break;
+          load_bias(nq);
+        }
       }
     }
     if (*abort_flag) {
       // let this CTA's own copies land before it retires (bounded waits)
       mbar_wait(&bars[kKVFull], 0, p.err, kDevErrTimeout, nullptr);
-      for (int m = n > 2 ? n - 2 : 0; m <= n; ++m) {
+      for (int m = n > 2 ? n - 2 : 0; m <= n; ++m)
         mbar_wait(&bars[kQFull + (m & 1)], (m >> 1) & 1, p.err, kDevErrTimeout, nullptr);
-        mbar_wait(&bars[kDoFull + m % DOS], (m / DOS) & 1, p.err, kDevErrTimeout, nullptr);
-      }
-      if (HAS_BIAS && qi_count > 0) mbar_wait(&bars[kBFull], (qi_count - 1) & 1, p.err, kDevErrTimeout, nullptr);
+      // only the last fill of each slot can still be in flight
+      if (ufill0 > 0) mbar_wait(&bars[kDoFull + 0], (ufill0 - 1) & 1, p.err, kDevErrTimeout, nullptr);
+      if (ufill1 > 0) mbar_wait(&bars[kDoFull + 1], (ufill1 - 1) & 1, p.err, kDevErrTimeout, nullptr);
+      if (HAS_BIAS && nbias > 0) mbar_wait(&bars[kBFull], (nbias - 1) & 1, p.err, kDevErrTimeout, nullptr);
     }
    } else if (warp == 1 && lane == 0 && any_active) {
     // ------------------------------------------------------------ MMA issuer
@@ -306,9 +337,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t do0desc_mn = sdesc_sw128(smem_u32(sDO), 16384, 1024);
     const uint64_t slot = static_cast<uint64_t>(L::kQB >> 4);
     int n = 0;
+    int uuse0 = 0, uuse1 = 0;  // dO uses of slot 0 / slot 1
     for (int qt = first_qt; ok && qt < p.nTq; qt = it.next(qt)) {
       for (int hh = 0; hh < p.G; ++hh, ++n) {
-        const int s = n & 1, sd = n % DOS;
+        const int s = n & 1, sd = do_slot<HAS_BIAS>(n, hh, p.G);
         if (!(ok = mbar_wait(&bars[kQFull + s], (n >> 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
         tc_fence_after();
         const uint64_t qdesc_k = q0desc_k + s * slot, qdesc_mn = q0desc_mn + s * slot;
@@ -319,7 +351,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           umma_ss(tbase, kdesc_k + kmajor_step(k, 128), qdesc_k + kmajor_step(k, 128), IDESC_S, k > 0);
         umma_commit(&bars[kSFull]);
         // dP^T = V dO^T into the columns the previous dQ used
-        if (!(ok = mbar_wait(&bars[kDoFull + sd], (n / DOS) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        if (!(ok = mbar_wait(&bars[kDoFull + sd], (sd ? uuse1 : uuse0) & 1, p.err, kDevErrTimeout, abort_flag))) break;
         if (n > 0 && !(ok = mbar_wait(&bars[kDqFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
         tc_fence_after();
 #pragma unroll
@@ -344,6 +376,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           umma_ts(tbase + 256, tbase + k * 8 + (k >= 4 ? 32 : 0), dodesc_mn + mnmajor_step(k), IDESC_DV,
                   (n > 0 || k > 0) ? 1u : 0u);
         umma_commit(&bars[kDoEmpty + sd]);
+        if (sd) ++uuse1;
+        else ++uuse0;
         // dK += dS^T Q
 #pragma unroll
         for (int k = 0; k < 8; ++k)
