@@ -45,40 +45,66 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ float bf16_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
 
 // ----------------------------------------------------------------------- preprocess
+// One warp per (batch, head, 32 query rows): delta_i = sum_d dO*O with 16 lanes per row
+// (8 bf16 per lane and load), then the 32 rows' -lse*log2(e) and delta are written by one
+// coalesced store each.  Each CTA also zeroes a contiguous share of the fp32 dQ accumulator.
+constexpr int kPreRowsPerWarp = 32;
+
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;  // (b, i, h), h fastest
-  const int64_t nrows = static_cast<int64_t>(p.B) * p.nqpad * p.Hq;
-  if (row >= nrows) return;
-  const int h = static_cast<int>(row % p.Hq);
-  const int64_t bi = row / p.Hq;
-  const int i = static_cast<int>(bi % p.nqpad);
-  const int b = static_cast<int>(bi / p.nqpad);
-  float acc = 0.f;
-  const bool valid = i < p.Nq;
-  if (valid) {
-    const int64_t off = ((static_cast<int64_t>(b) * p.Nq + i) * p.Hq + h) * p.d;
-    for (int c = lane * 4; c < p.d; c += 128) {
-      const uint2 o = *reinterpret_cast<const uint2*>(p.out + off + c);
-      const uint2 g = *reinterpret_cast<const uint2*>(p.dout + off + c);
-      acc += bf16_to_f32(o.x & 0xFFFFu) * bf16_to_f32(g.x & 0xFFFFu) + bf16_to_f32(o.x >> 16) * bf16_to_f32(g.x >> 16) +
-             bf16_to_f32(o.y & 0xFFFFu) * bf16_to_f32(g.y & 0xFFFFu) + bf16_to_f32(o.y >> 16) * bf16_to_f32(g.y >> 16);
-    }
-  }
+  const int nblk = (p.nqpad + kPreRowsPerWarp - 1) / kPreRowsPerWarp;
+  const int64_t task = static_cast<int64_t>(blockIdx.x) * 8 + warp;  // (b, h, row block), row block fastest
+  const int64_t ntask = static_cast<int64_t>(p.B) * p.Hq * nblk;
+  if (task < ntask) {
+    const int blk = static_cast<int>(task % nblk);
+    const int64_t bh = task / nblk;
+    const int h = static_cast<int>(bh % p.Hq);
+    const int b = static_cast<int>(bh / p.Hq);
+    const int i0 = blk * kPreRowsPerWarp;
+    const int half = lane >> 4, l16 = lane & 15;
+    float mine = 0.f;  // delta of row i0 + lane
+#pragma unroll 4
+    for (int r = 0; r < kPreRowsPerWarp; r += 2) {
+      const int i = i0 + r + half;
+      float acc = 0.f;
+      if (i < p.Nq) {
+        const int64_t off = ((static_cast<int64_t>(b) * p.Nq + i) * p.Hq + h) * p.d;
+        for (int c = l16 * 8; c < p.d; c += 128) {
+          const uint4 o = *reinterpret_cast<const uint4*>(p.out + off + c);
+          const uint4 g = *reinterpret_cast<const uint4*>(p.dout + off + c);
+          const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  float* dq = p.dq_acc + row * p.d;
-  for (int c = lane * 4; c < p.d; c += 128) *reinterpret_cast<float4*>(dq + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (lane == 0) {
-    const int64_t o = (static_cast<int64_t>(b) * p.Hq + h) * p.nqpad + i;
-    float l2 = -kPosInf;
-    if (valid) {
-      const float l = p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + i];
-      l2 = (l == -kPosInf) ? -kPosInf : -(l * kLog2e);
+          for (int q = 0; q < 4; ++q)
+            acc += bf16_to_f32(ow[q] & 0xFFFFu) * bf16_to_f32(gw[q] & 0xFFFFu) +
+                   bf16_to_f32(ow[q] >> 16) * bf16_to_f32(gw[q] >> 16);
+        }
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);  // within each half
+      const float v0 = __shfl_sync(0xffffffffu, acc, 0), v1 = __shfl_sync(0xffffffffu, acc, 16);
+      if (lane == r) mine = v0;
+      if (lane == r + 1) mine = v1;
     }
-    p.lse2[o] = l2;
-    p.delta[o] = valid ? acc : 0.f;
+    const int i = i0 + lane;
+    if (i < p.nqpad) {
+      const int64_t o = (static_cast<int64_t>(b) * p.Hq + h) * p.nqpad + i;
+      const bool valid = i < p.Nq;
+      float l2 = -kPosInf;
+      if (valid) {
+        const float l = p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + i];
+        l2 = (l == -kPosInf) ? -kPosInf : -(l * kLog2e);
+      }
+      p.lse2[o] = l2;
+      p.delta[o] = valid ? mine : 0.f;
+    }
   }
+  // zero this CTA's contiguous share of the dQ accumulator (B, nqpad, Hq, d) fp32
+  const int64_t total4 = static_cast<int64_t>(p.B) * p.nqpad * p.Hq * p.d / 4;
+  const int64_t per = (total4 + gridDim.x - 1) / gridDim.x;
+  const int64_t z0 = static_cast<int64_t>(blockIdx.x) * per;
+  const int64_t z1 = min(total4, z0 + per);
+  float4* z = reinterpret_cast<float4*>(p.dq_acc);
+  for (int64_t k = z0 + threadIdx.x; k < z1; k += blockDim.x) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 __global__ void __launch_bounds__(256) dq_convert_kernel(const DqConvertParams p) {
@@ -659,8 +685,8 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 }  // namespace
 
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream) {
-  const int64_t rows = static_cast<int64_t>(p.B) * p.nqpad * p.Hq;
-  bwd_pre_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
+  const int64_t tasks = static_cast<int64_t>(p.B) * p.Hq * ((p.nqpad + kPreRowsPerWarp - 1) / kPreRowsPerWarp);
+  bwd_pre_kernel<<<static_cast<unsigned>((tasks + 7) / 8), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

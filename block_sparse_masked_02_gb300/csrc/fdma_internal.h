@@ -54,7 +54,7 @@ struct BwdPreParams {
   const uint16_t* out;
   const uint16_t* dout;
   const float* lse;
-  float* lse2;   // (B,Hq,nqpad): lse*log2(e), +inf for empty / padded rows
+  float* lse2;   // (B,Hq,nqpad): -lse*log2(e), -inf for empty / padded rows
   float* delta;  // (B,Hq,nqpad)
   float* dq_acc; // (B,nqpad,Hq,d), zeroed
 };
