@@ -364,30 +364,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t slot = static_cast<uint64_t>(L::kQB >> 4);
     int n = 0;
     int uuse0 = 0, uuse1 = 0;  // dO uses of slot 0 / slot 1
+    // S^T of step m (query slot m & 1); false after a failed wait
+    auto issue_s = [&](int m) -> bool {
+      const int s = m & 1;
+      if (!mbar_wait(&bars[kQFull + s], (m >> 1) & 1, p.err, kDevErrTimeout, abort_flag)) return false;
+      tc_fence_after();
+      const uint64_t qdesc_k = q0desc_k + s * slot;
+      // S^T = K Q^T
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k)
+        umma_ss(tbase, kdesc_k + kmajor_step(k, 128), qdesc_k + kmajor_step(k, 128), IDESC_S, k > 0);
+      umma_commit(&bars[kSFull]);
+      return true;
+    };
+    // dP^T of step m (dO slot sd), into the columns the previous dQ used
+    auto issue_dp = [&](int m, int sd) -> bool {
+      const uint64_t dodesc_k = do0desc_k + sd * slot;
+      if (!mbar_wait(&bars[kDoFull + sd], (sd ? uuse1 : uuse0) & 1, p.err, kDevErrTimeout, abort_flag)) return false;
+      if (m > 0 && !mbar_wait(&bars[kDqFree], (m - 1) & 1, p.err, kDevErrTimeout, abort_flag)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k)
+        umma_ss(tbase + 128, vdesc_k + kmajor_step(k, 128), dodesc_k + kmajor_step(k, 128), IDESC_S, k > 0);
+      umma_commit(&bars[kDpFull]);
+      return true;
+    };
+    // Per step n: dQ(n), dV(n), S^T(n+1), dK(n), dP^T(n+1).  S^T(n+1) needs only dV(n) to have
+    // read P^T(n) and dP^T(n+1) only the drain of dQ(n), which dK(n) overlaps; the next step's
+    // inputs are then ready while this step's dQ is still being reduced.
+    ok = ok && issue_s(0) && issue_dp(0, do_slot<HAS_BIAS>(0, 0, p.G));
     for (int qt = first_qt; ok && qt < p.nTq; qt = it.next(qt)) {
       for (int hh = 0; hh < p.G; ++hh, ++n) {
         const int s = n & 1, sd = do_slot<HAS_BIAS>(n, hh, p.G);
-        if (!(ok = mbar_wait(&bars[kQFull + s], (n >> 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
-        tc_fence_after();
-        const uint64_t qdesc_k = q0desc_k + s * slot, qdesc_mn = q0desc_mn + s * slot;
-        const uint64_t dodesc_k = do0desc_k + sd * slot, dodesc_mn = do0desc_mn + sd * slot;
-        // S^T = K Q^T
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          umma_ss(tbase, kdesc_k + kmajor_step(k, 128), qdesc_k + kmajor_step(k, 128), IDESC_S, k > 0);
-        umma_commit(&bars[kSFull]);
-        // dP^T = V dO^T into the columns the previous dQ used
-        if (!(ok = mbar_wait(&bars[kDoFull + sd], (sd ? uuse1 : uuse0) & 1, p.err, kDevErrTimeout, abort_flag))) break;
-        if (n > 0 && !(ok = mbar_wait(&bars[kDqFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          umma_ss(tbase + 128, vdesc_k + kmajor_step(k, 128), dodesc_k + kmajor_step(k, 128), IDESC_S, k > 0);
-        umma_commit(&bars[kDpFull]);
+        const uint64_t qdesc_mn = q0desc_mn + s * slot, dodesc_mn = do0desc_mn + sd * slot;
         if (!(ok = mbar_wait(&bars[kPReady], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
         tc_fence_after();
         // dQ first (K dimension = 128 keys; written over the dP^T columns, which the compute
-        // warps have read): its drain then overlaps the dV / dK products below
+        // warps have read): its drain then overlaps the products below
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           if (DQ_T)
@@ -404,6 +417,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         umma_commit(&bars[kDoEmpty + sd]);
         if (sd) ++uuse1;
         else ++uuse0;
+        const bool more = hh + 1 < p.G || it.next(qt) < p.nTq;
+        if (more && !(ok = issue_s(n + 1))) break;
         // dK += dS^T Q
 #pragma unroll
         for (int k = 0; k < 8; ++k)
@@ -411,6 +426,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                   (n > 0 || k > 0) ? 1u : 0u);
         umma_commit(&bars[kQEmpty + s]);
         umma_commit(&bars[kDsFree]);
+        if (more) {
+          const int hn = hh + 1 < p.G ? hh + 1 : 0;
+          if (!(ok = issue_dp(n + 1, do_slot<HAS_BIAS>(n + 1, hn, p.G)))) break;
+        }
       }
     }
     umma_commit(&bars[kFinal]);
