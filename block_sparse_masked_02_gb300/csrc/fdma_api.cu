@@ -52,7 +52,7 @@ int validate(const fdma_args* a, bool need_workspace) {
   if (a == nullptr) return FDMA_ERR_INVALID;
   if (a->B <= 0 || a->Nq <= 0 || a->Nk <= 0 || a->Hq <= 0 || a->Hkv <= 0) return FDMA_ERR_INVALID;
   if (a->Hq % a->Hkv != 0) return FDMA_ERR_INVALID;
-  if (a->d != 64 && a->d != 128) return FDMA_ERR_UNSUPPORTED;
+  if (!head_dim_ok(a->d)) return FDMA_ERR_UNSUPPORTED;
   if (cdiv(a->Nk, kTile) > kMaxKTiles || cdiv(a->Nq, kTile) > kMaxKTiles) return FDMA_ERR_UNSUPPORTED;
   if (!(std::isfinite(a->scale) && a->scale > 0.f)) return FDMA_ERR_INVALID;
   if (a->q == nullptr || a->k == nullptr || a->v == nullptr) return FDMA_ERR_INVALID;
@@ -185,7 +185,7 @@ WorkspaceLayout workspace_layout(int B, int Nq, int Nk, int Hq, int Hkv, int d) 
   w.delta = off;
   off = align256(off + static_cast<size_t>(B) * Hq * nqpad * 4);
   w.dq_acc = off;
-  off = align256(off + static_cast<size_t>(B) * nqpad * Hq * d * 4);
+  off = align256(off + static_cast<size_t>(B) * nqpad * Hq * padded_head_dim(d) * 4);
   w.total_bwd = off;
   return w;
 }
@@ -198,7 +198,7 @@ extern "C" {
 
 size_t fdma_workspace_size(const fdma_args* a, int for_bwd) {
   if (a == nullptr || a->B <= 0 || a->Nq <= 0 || a->Nk <= 0 || a->Hq <= 0 || a->Hkv <= 0 || a->Hq % a->Hkv ||
-      (a->d != 64 && a->d != 128))
+      !head_dim_ok(a->d))
     return 0;
   const WorkspaceLayout w = workspace_layout(a->B, a->Nq, a->Nk, a->Hq, a->Hkv, a->d);
   return for_bwd ? w.total_bwd : w.total_fwd;
@@ -245,6 +245,7 @@ int fdma_fwd(const fdma_args* a, void* out, float* lse, void* stream_v) {
   p.Hq = a->Hq;
   p.Hkv = a->Hkv;
   p.G = a->Hq / a->Hkv;
+  p.d = a->d;
   p.nTq = cdiv(a->Nq, kTile);
   p.nTk = cdiv(a->Nk, kTile);
   p.scale = a->scale;
@@ -256,7 +257,8 @@ int fdma_fwd(const fdma_args* a, void* out, float* lse, void* stream_v) {
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   p.err = err;
-  return launch_fwd(a->d, has_bias, tq, tk, tv, tb, p, stream) == cudaSuccess ? FDMA_OK : FDMA_ERR_CUDA;
+  return launch_fwd(padded_head_dim(a->d), has_bias, tq, tk, tv, tb, p, stream) == cudaSuccess ? FDMA_OK
+                                                                                               : FDMA_ERR_CUDA;
 }
 
 int fdma_bwd(const fdma_args* a, const void* out, const void* dout, const float* lse, void* dq, void* dk, void* dv,
@@ -288,6 +290,7 @@ int fdma_bwd(const fdma_args* a, const void* out, const void* dout, const float*
   pp.Nq = a->Nq;
   pp.Hq = a->Hq;
   pp.d = a->d;
+  pp.dpad = padded_head_dim(a->d);
   pp.nqpad = nqpad;
   pp.out = static_cast<const uint16_t*>(out);
   pp.dout = static_cast<const uint16_t*>(dout);
@@ -311,6 +314,7 @@ int fdma_bwd(const fdma_args* a, const void* out, const void* dout, const float*
   p.Hq = a->Hq;
   p.Hkv = a->Hkv;
   p.G = a->Hq / a->Hkv;
+  p.d = a->d;
   p.nTq = nTq;
   p.nTk = nTk;
   p.nqpad = nqpad;
@@ -343,13 +347,15 @@ int fdma_bwd(const fdma_args* a, const void* out, const void* dout, const float*
                             static_cast<uint64_t>(a->Hkv) * a->Nq * a->Nk * 2};
     if (!make_map(&tdb, dbias, dims, sb)) return FDMA_ERR_UNSUPPORTED;
   }
-  if (launch_bwd(a->d, a->bias != nullptr, dbias != nullptr, tq, tk, tv, tdo, tb, tdb, p, stream) != cudaSuccess)
+  if (launch_bwd(padded_head_dim(a->d), a->bias != nullptr, dbias != nullptr, tq, tk, tv, tdo, tb, tdb, p, stream) !=
+      cudaSuccess)
     return FDMA_ERR_CUDA;
   DqConvertParams cp{};
   cp.B = a->B;
   cp.Nq = a->Nq;
   cp.Hq = a->Hq;
   cp.d = a->d;
+  cp.dpad = padded_head_dim(a->d);
   cp.nqpad = nqpad;
   cp.dq_acc = pp.dq_acc;
   cp.dq = static_cast<uint16_t*>(dq);

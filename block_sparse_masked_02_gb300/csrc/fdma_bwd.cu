@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
     }
   }
   // zero this CTA's contiguous share of the dQ accumulator (B, nqpad, Hq, d) fp32
-  const int64_t total4 = static_cast<int64_t>(p.B) * p.nqpad * p.Hq * p.d / 4;
+  const int64_t total4 = static_cast<int64_t>(p.B) * p.nqpad * p.Hq * p.dpad / 4;
   const int64_t per = (total4 + gridDim.x - 1) / gridDim.x;
   const int64_t z0 = static_cast<int64_t>(blockIdx.x) * per;
   const int64_t z1 = min(total4, z0 + per);
@@ -113,7 +113,8 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const DqConvertParams p
   if (idx >= total) return;
   const int64_t per_b = static_cast<int64_t>(p.Nq) * p.Hq * p.d;
   const int64_t b = idx / per_b, rest = idx % per_b;
-  const float* src = p.dq_acc + b * static_cast<int64_t>(p.nqpad) * p.Hq * p.d + rest;
+  const int64_t row = rest / p.d, col = rest % p.d;  // (i, h) and head-dim column (8 per thread)
+  const float* src = p.dq_acc + (b * static_cast<int64_t>(p.nqpad) * p.Hq + row) * p.dpad + col;
   const float4 a = *reinterpret_cast<const float4*>(src);
   const float4 c = *reinterpret_cast<const float4*>(src + 4);
   *reinterpret_cast<uint4*>(p.dq + idx) =
@@ -581,16 +582,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // instruction adds 32 consecutive floats of one query row
           const int64_t rstride = static_cast<int64_t>(p.Hq) * D;
           float* dst = p.dq_acc + ((static_cast<int64_t>(b) * p.nqpad + q0 + qbase) * p.Hq + h) * D + j;
+          if (j < p.d) {  // head-dim rows past d are padding (zero)
 #pragma unroll
-          for (int t = 0; t < 32; ++t, dst += rstride) red_add_f32(dst, __uint_as_float(r0[t]) * p.scale);
+            for (int t = 0; t < 32; ++t, dst += rstride) red_add_f32(dst, __uint_as_float(r0[t]) * p.scale);
 #pragma unroll
-          for (int t = 0; t < 32; ++t, dst += rstride) red_add_f32(dst, __uint_as_float(r1[t]) * p.scale);
+            for (int t = 0; t < 32; ++t, dst += rstride) red_add_f32(dst, __uint_as_float(r1[t]) * p.scale);
+          }
         } else {
           float* dqrow = p.dq_acc + ((static_cast<int64_t>(b) * p.nqpad + q0 + j) * p.Hq + h) * D + wg * (D / 2);
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            red_add_v4(dqrow + 4 * v, __uint_as_float(r0[4 * v]) * p.scale, __uint_as_float(r0[4 * v + 1]) * p.scale,
-                       __uint_as_float(r0[4 * v + 2]) * p.scale, __uint_as_float(r0[4 * v + 3]) * p.scale);
+            if (wg * (D / 2) + 4 * v < p.d)
+              red_add_v4(dqrow + 4 * v, __uint_as_float(r0[4 * v]) * p.scale,
+                         __uint_as_float(r0[4 * v + 1]) * p.scale, __uint_as_float(r0[4 * v + 2]) * p.scale,
+                         __uint_as_float(r0[4 * v + 3]) * p.scale);
         }
       }
       if (WANT_DBIAS) {
@@ -647,7 +652,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // dK (warpgroup 0) and dV (warpgroup 1)
     if (ok) {
       tc_fence_after();
-      const int64_t off = ((static_cast<int64_t>(b) * p.Nk + kidx) * p.Hkv + g) * D;
+      const int64_t off = ((static_cast<int64_t>(b) * p.Nk + kidx) * p.Hkv + g) * p.d;
       uint16_t* dst = (wg == 0 ? p.dk : p.dv) + off;
       const uint32_t col0 = wg == 0 ? 384u : 256u;
       const float sc = wg == 0 ? p.scale : 1.f;
@@ -665,10 +670,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int t = 0; t < 16; ++t)
           pk[t] = pack_bf16x2(__uint_as_float(r[2 * t]) * sc, __uint_as_float(r[2 * t + 1]) * sc);
-        if (kin) {
+        if (kin) {  // columns past the head dim are padding
           uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          for (int v = 0; v < 4; ++v)
+            if (c * 32 + v * 8 < p.d) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
     }

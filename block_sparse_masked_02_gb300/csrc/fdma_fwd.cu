@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(192, 1)
     if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint16_t* orow = p.out + ((static_cast<int64_t>(b) * p.Nq + i) * p.Hq + h) * D;
+      uint16_t* orow = p.out + ((static_cast<int64_t>(b) * p.Nq + i) * p.Hq + h) * p.d;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         if (n > 0) {
@@ -363,10 +363,11 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j)
           pk[j] = pack_bf16x2(__uint_as_float(raw[2 * j]) * inv, __uint_as_float(raw[2 * j + 1]) * inv);
-        if (i < p.Nq) {
+        if (i < p.Nq) {  // columns past the head dim are padding
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          for (int v = 0; v < 4; ++v)
+            if (c * 32 + v * 8 < p.d) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
       if (i < p.Nq)
@@ -764,7 +765,7 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
     if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint16_t* orow = p.out + ((static_cast<int64_t>(b) * p.Nq + i) * p.Hq + h) * D;
+      uint16_t* orow = p.out + ((static_cast<int64_t>(b) * p.Nq + i) * p.Hq + h) * p.d;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         if (n > 0) {
@@ -778,10 +779,11 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j)
           pk[j] = pack_bf16x2(__uint_as_float(raw[2 * j]) * inv, __uint_as_float(raw[2 * j + 1]) * inv);
-        if (i < p.Nq) {
+        if (i < p.Nq) {  // columns past the head dim are padding
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          for (int v = 0; v < 4; ++v)
+            if (c * 32 + v * 8 < p.d) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
       if (i < p.Nq)

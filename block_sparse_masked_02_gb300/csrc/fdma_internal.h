@@ -14,6 +14,14 @@ namespace fdma {
 constexpr int kTile = 128;           // query rows and key columns per tile
 constexpr int kMaxKTiles = 1024;     // Nk <= 131072
 constexpr int kTopkMaxKeys = 65536;  // one row's keys held in shared memory
+
+// Head dims 64 and 72..128 (multiples of 8).  A head dim between 64 and 128 runs on the
+// kernels for 128: the TMA load of its upper 64-column box zero-fills the columns past d,
+// which then add nothing to any product, and nothing is stored past column d.  (Head dims
+// below 64 would need 64-byte-swizzled tiles: the 64-column box cannot be wider than the
+// tensor.)
+inline int padded_head_dim(int d) { return d <= 64 ? 64 : 128; }
+inline bool head_dim_ok(int d) { return d == 64 || (d > 64 && d <= 128 && d % 8 == 0); }
 constexpr int kSkip = 0, kPartial = 1, kFull = 2;
 
 // Device error word values (first writer wins).
@@ -40,6 +48,7 @@ struct ClassifyParams {
 
 struct FwdParams {
   int B, Nq, Nk, Hq, Hkv, G, nTq, nTk;
+  int d;  // head dim of q, k, v, out (the kernel runs on its padded width, 64 or 128)
   int bias_bsel, bias_hsel;  // 0 where the bias is broadcast over batch / kv head (TMA coordinate 0)
   float scale, scale_log2;  // softmax scale and scale * log2(e)
   const int8_t* kmap;
@@ -51,6 +60,7 @@ struct FwdParams {
 
 struct BwdPreParams {
   int B, Nq, Hq, d, nqpad;
+  int dpad;  // row width of the dQ accumulator (64 or 128)
   const uint16_t* out;
   const uint16_t* dout;
   const float* lse;
@@ -61,6 +71,7 @@ struct BwdPreParams {
 
 struct BwdParams {
   int B, Nq, Nk, Hq, Hkv, G, nTq, nTk, nqpad;
+  int d;  // head dim of q, k, v, dout, dk, dv (the kernel runs on its padded width)
   int bias_bsel, bias_hsel;  // 0 where the bias is broadcast over batch / kv head (TMA coordinate 0)
   float scale, scale_log2;
   const int8_t* kmap;
@@ -78,6 +89,7 @@ struct BwdParams {
 
 struct DqConvertParams {
   int B, Nq, Hq, d, nqpad;
+  int dpad;  // row width of the dQ accumulator
   const float* dq_acc;
   uint16_t* dq;
 };

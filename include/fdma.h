@@ -79,7 +79,8 @@ typedef enum {
 #define FDMA_FLAG_NO_SKIP 2u              /* debug: treat every causally allowed tile as PARTIAL (no skipping) */
 
 typedef struct fdma_args {
-  /* problem size: batch, query length, key length, query heads, kv heads, head dim (64 or 128) */
+  /* problem size: batch, query length, key length, query heads, kv heads, head dim (64, or a
+     multiple of 8 from 72 to 128; other values: FDMA_ERR_UNSUPPORTED) */
   int32_t B, Nq, Nk, Hq, Hkv, d;
 
   /* q (B,Nq,Hq,d), k and v (B,Nk,Hkv,d); strides in ELEMENTS for (batch, seq, head); the

@@ -311,8 +311,8 @@ def test_argument_errors(F):
         F.fwd(q3, torch.zeros(1, 128, 2, 64, dtype=torch.bfloat16, device="cuda"),
               torch.zeros(1, 128, 2, 64, dtype=torch.bfloat16, device="cuda"))
     assert e.value.status == F.FDMA_ERR_INVALID
-    q96 = torch.zeros(1, 128, 2, 96, dtype=torch.bfloat16, device="cuda")
-    k96 = torch.zeros(1, 128, 1, 96, dtype=torch.bfloat16, device="cuda")
+    q96 = torch.zeros(1, 128, 2, 100, dtype=torch.bfloat16, device="cuda")  # head dim not a multiple of 8
+    k96 = torch.zeros(1, 128, 1, 100, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(F.FdmaError) as e:
         F.fwd(q96, k96, k96)
     assert e.value.status == F.FDMA_ERR_UNSUPPORTED
@@ -367,3 +367,13 @@ def test_bit_packed_mask(F):
     rq, rk, rv, _ = orc.backward(p, want_dbias=False)
     for name, x, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
         assert rel_l2(x.float().cpu().numpy(), ref) <= G_RELL2, name
+
+
+@pytest.mark.parametrize("d,Hq,Hkv", [(72, 4, 2), (80, 4, 2), (96, 3, 1), (120, 4, 2), (80, 3, 1)])
+def test_other_head_dims(F, d, Hq, Hkv):
+    """Head dims between 64 and 128 (multiples of 8) run on the 128-wide kernels: outputs
+    and gradients match the oracle (which also checks their shapes: nothing past column d)."""
+    wl = W.scaled(W.WORKLOADS["n4096_hq32_hkv8"], Nq=296, Nk=296, Hq=Hq, Hkv=Hkv, d=d, keep_window=96,
+                  seed=40 + d + Hq, scale=1.0 / math.sqrt(d))
+    inp = W.make_inputs(wl)
+    run_and_compare(F, inp, True, wl.scale)

@@ -70,12 +70,15 @@ def test_workspace_size_arithmetic(F):
     tiles = 1 * 2 * 2 * 2
     assert fwd >= tiles + 2 * tiles * 128 * 16
     assert bwd >= fwd + 2 * (4 * 256 * 4) + 256 * 4 * 128 * 4
-    assert lib.fdma_workspace_size(ctypes.byref(_args(F, d=96)), 0) == 0
+    assert lib.fdma_workspace_size(ctypes.byref(_args(F, d=100)), 0) == 0
+    # d = 96 runs on the 128-wide kernels: its dQ accumulator rows are 128 floats wide
+    assert lib.fdma_workspace_size(ctypes.byref(_args(F, d=96)), 1) == bwd
     assert lib.fdma_workspace_size(ctypes.byref(_args(F, Hq=3)), 0) == 0
 
 
 @pytest.mark.parametrize("field,value,status", [
-    ("scale", float("nan"), 1), ("scale", -1.0, 1), ("Hq", 3, 1), ("d", 96, 2), ("Nk", 0, 1),
+    ("scale", float("nan"), 1), ("scale", -1.0, 1), ("Hq", 3, 1), ("d", 100, 2), ("d", 136, 2), ("d", 32, 2),
+    ("Nk", 0, 1),
     ("mask_kind", 7, 1), ("mask_kind", 1, 1), ("mask_kind", 3, 1), ("mask_kind", 4, 1), ("Hkv", 0, 1),
 ])
 def test_argument_validation_before_any_cuda_call(F, field, value, status):
