@@ -34,9 +34,9 @@ METRIC = "effective fwd+bwd TFLOP/s (non-skipped tiles) and % of roofline, 1 GB3
 TILE = 128
 KERNELS_PER_STEP = 5  # classify, fwd, bwd_pre, bwd, dq_convert
 # DRAM bytes (read + write) of one bwd_kernel launch on this workload: an ncu capture of
-# bwd_kernel on n4096_hq32_hkv8 (334.46 MB read + 304.33 MB written) scaled by the active
+# bwd_kernel on n4096_hq32_hkv8 (334.45 MB read + 304.22 MB written) scaled by the active
 # (tile, head) units, 132096 / 16896; None whenever the kernel has changed since that capture.
-BWD_TRAFFIC_BYTES = round((334.456320e6 + 304.328192e6) * 132096 / 16896)
+BWD_TRAFFIC_BYTES = round((334.453504e6 + 304.215552e6) * 132096 / 16896)
 
 
 def _peaks():

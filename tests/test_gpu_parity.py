@@ -377,3 +377,11 @@ def test_other_head_dims(F, d, Hq, Hkv):
                   seed=40 + d + Hq, scale=1.0 / math.sqrt(d))
     inp = W.make_inputs(wl)
     run_and_compare(F, inp, True, wl.scale)
+
+
+def test_one_head_per_kv_head_with_bias(F):
+    """G = 1 with a bias: the backward keeps one dO slot and reloads the bias buffer after each
+    query tile's bias copy (no second dO slot to alternate with)."""
+    wl = W.scaled(W.WORKLOADS["n4096_hq32_hkv8"], Nq=392, Nk=392, Hq=2, Hkv=2, keep_window=128, seed=53)
+    inp = W.make_inputs(wl)
+    run_and_compare(F, inp, True, wl.scale)
