@@ -3,15 +3,16 @@
 // Features": forward and backward share the block skip decisions and dBias
 // is fused into the backward).
 //
-//   bwd_pre_kernel   delta_i = <dO_i, O_i>, lse in log2 units (+inf for rows
-//                    with no kept key and for padding), zero the fp32 dQ
-//                    accumulator.
+//   bwd_pre_kernel   delta_i = <dO_i, O_i> and -lse*log2(e) (-inf for rows with no
+//                    kept key and for padding), 32 rows of one head per warp with
+//                    coalesced stores; zeroes the fp32 dQ accumulator.
 //   bwd_kernel       one CTA = (batch, kv head, 128-key tile).  For every
-//                    active query tile (column of the block map) and every
-//                    query head of the GQA group:
+//                    active query tile (column of the block map, copied into shared
+//                    memory) and every query head of the GQA group, one step:
 //                      S^T  = K Q^T           (SS, TMEM cols   0..127)
 //                      dP^T = V dO^T          (SS, TMEM cols 128..255)
-//                      P^T  = exp2(S^T*c + bias^T*log2e - lse2)   (mask bits)
+//                      P^T  = exp2(S^T*c + bias^T*log2e - lse2)   (-inf bias at masked
+//                                              pairs, or the keep bits without a bias)
 //                      dS^T = P^T (dP^T - delta)
 //                      dV  += P^T dO          (TS: P^T packed in TMEM cols 0..31, 64..95)
 //                      dK  += dS^T Q          (SS: dS^T staged in smem)
@@ -19,13 +20,17 @@
 //                                              d = 128 computed as dQ^T = K^T dS^T so
 //                                              that each warp's reduction covers 32
 //                                              consecutive floats of one row)
-//                    dQ is added to an fp32 accumulator with reductions; dBias = sum over the group's heads of dS is
-//                    kept in registers (one thread per key and half of the
-//                    query tile) and written once per (query tile, key tile);
-//                    the bias tile of a query tile is TMA-loaded into shared
-//                    memory once and each thread copies its key column into
-//                    registers for all heads; skipped tiles of dBias are written as zeros by the
-//                    same CTA.  Warps: 0 TMA, 1 MMA, 4..11 two compute groups.
+//                    MMA order per step: dQ, dV, next S^T, dK, next dP^T.  dQ is added
+//                    to an fp32 accumulator with reductions by the compute warps; dBias
+//                    = sum over the group's heads of dS is kept in registers (one
+//                    thread per key and half of the query tile) and written once per
+//                    (query tile, key tile) through a staged TMA store; the bias tile
+//                    of a query tile is TMA-loaded into shared memory once and each
+//                    thread copies its key column into registers for all heads, while
+//                    the previous tile's last head waits for its dQ product.  dO is
+//                    double-buffered (with a bias, the second slot is the bias buffer).
+//                    Skipped tiles of dBias are written as zeros by the same CTA.
+//                    Warps: 0 TMA, 1 MMA, 4..11 two compute groups.
 //   dq_convert       fp32 accumulator -> bf16 dQ.
 #include "fdma_internal.h"
 #include "fdma_ptx.cuh"
