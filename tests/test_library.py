@@ -119,3 +119,19 @@ def test_pack_mask_matches_numpy_packbits(F):
         pm = F.pack_mask(m)
         ref = np.packbits((m != 0).numpy(), axis=-1, bitorder="little")
         assert pm.nk == nk and np.array_equal(pm.bits.numpy(), ref)
+
+
+def test_binding_refuses_cpu_tensors_and_bad_packed_masks(F):
+    import torch
+    bias = torch.zeros(1, 1, 4, 16, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensors only"):
+        F.topk_mask(bias, 4)
+    q = torch.zeros(1, 128, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensors only"):
+        F.fwd(q, q[:, :, :1], q[:, :, :1])
+    with pytest.raises(ValueError):
+        F.PackedMask(torch.zeros(1, 1, 4, 2, dtype=torch.int32), 16)  # not uint8
+    with pytest.raises(ValueError):
+        F.PackedMask(torch.zeros(1, 1, 4, 3, dtype=torch.uint8), 16)  # ceil(16/8) = 2 bytes per row
+    pm = F.PackedMask(torch.zeros(1, 1, 4, 3, dtype=torch.uint8), 17)
+    assert pm.nk == 17 and not pm.is_cuda
