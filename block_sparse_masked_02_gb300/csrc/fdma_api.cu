@@ -292,6 +292,7 @@ int fdma_bwd(const fdma_args* a, const void* out, const void* dout, const float*
   pp.d = a->d;
   pp.dpad = padded_head_dim(a->d);
   pp.nqpad = nqpad;
+  pp.scale = a->scale;
   pp.out = static_cast<const uint16_t*>(out);
   pp.dout = static_cast<const uint16_t*>(dout);
   pp.lse = lse;

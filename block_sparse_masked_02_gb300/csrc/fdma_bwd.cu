@@ -13,24 +13,27 @@
 //                      dP^T = V dO^T          (SS, TMEM cols 128..255)
 //                      P^T  = exp2(S^T*c + bias^T*log2e - lse2)   (-inf bias at masked
 //                                              pairs, or the keep bits without a bias)
-//                      dS^T = P^T (dP^T - delta)
+//                      scale*dS^T = P^T (scale*dP^T - scale*delta)
 //                      dV  += P^T dO          (TS: P^T packed in TMEM cols 0..31, 64..95)
-//                      dK  += dS^T Q          (SS: dS^T staged in smem)
-//                      dQ   = dS K            (SS, reuses TMEM cols 128..; for
-//                                              d = 128 computed as dQ^T = K^T dS^T so
-//                                              that each warp's reduction covers 32
-//                                              consecutive floats of one row)
-//                    MMA order per step: dQ, dV, next S^T, dK, next dP^T.  dQ is added
-//                    to an fp32 accumulator with reductions by the compute warps; dBias
-//                    = sum over the group's heads of dS is kept in registers (one
-//                    thread per key and half of the query tile) and written once per
-//                    (query tile, key tile) through a staged TMA store; the bias tile
-//                    of a query tile is TMA-loaded into shared memory once and each
-//                    thread copies its key column into registers for all heads, while
-//                    the previous tile's last head waits for its dQ product.  dO is
+//                      dK  += dS^T Q          (TS: dS^T packed in TMEM cols 128..159, 192..223)
+//                      dQ^T = K^T dS^T        (SS: dS^T also staged in smem; TMEM cols 128..;
+//                                              for d = 64 computed as dQ = dS K)
+//                    Four roles: a TMA producer, a single-thread MMA issuer, two compute
+//                    warpgroups and a dQ drain warpgroup.  The compute warps run each step
+//                    in two passes, P (right after S^T) and dS (after dP^T); the MMA order
+//                    per step is dV(n) once P^T(n) is stored, then S^T(n+1), dK(n), dQ(n),
+//                    dP^T(n+1) once dS^T(n) is stored, so the next step's P pass overlaps
+//                    the products.  The drain warps read dQ out of TMEM and add it to an fp32
+//                    accumulator with paced 16-byte reductions.  The softmax scale is folded
+//                    into dS (delta comes scaled from the preprocess), so dQ and dK need no
+//                    further scaling.  dBias = sum over the group's heads of dS is kept in
+//                    registers (one thread per key and half of the query tile) and written
+//                    once per (query tile, key tile) through a staged TMA store; the bias
+//                    tile of a query tile is TMA-loaded into shared memory once and each
+//                    thread copies its key column into registers for all heads.  dO is
 //                    double-buffered (with a bias, the second slot is the bias buffer).
 //                    Skipped tiles of dBias are written as zeros by the same CTA.
-//                    Warps: 0 TMA, 1 MMA, 4..11 two compute groups.
+//                    Warps: 0 TMA, 1 MMA, 4..11 two compute groups, 12..15 dQ drain.
 //   dq_convert       fp32 accumulator -> bf16 dQ.
 #include "fdma_internal.h"
 #include "fdma_ptx.cuh"
@@ -100,10 +103,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
         l2 = (l == -kPosInf) ? -kPosInf : -(l * kLog2e);
       }
       p.lse2[o] = l2;
-      p.delta[o] = valid ? mine : 0.f;
+      p.delta[o] = valid ? -p.scale * mine : 0.f;
     }
   }
-  // zero this CTA's contiguous share of the dQ accumulator (B, nqpad, Hq, d) fp32
+  // zero this CTA's contiguous share of the fp32 dQ accumulator
   const int64_t total4 = static_cast<int64_t>(p.B) * p.nqpad * p.Hq * p.dpad / 4;
   const int64_t per = (total4 + gridDim.x - 1) / gridDim.x;
   const int64_t z0 = static_cast<int64_t>(blockIdx.x) * per;
@@ -112,6 +115,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
   for (int64_t k = z0 + threadIdx.x; k < z1; k += blockDim.x) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// 64-wide accumulator (B, nqpad, Hq, 64): one thread per 8 consecutive dQ elements.
 __global__ void __launch_bounds__(256) dq_convert_kernel(const DqConvertParams p) {
   const int64_t idx = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 8;  // element of (b, i, h, d)
   const int64_t total = static_cast<int64_t>(p.B) * p.Nq * p.Hq * p.d;
@@ -126,6 +130,41 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const DqConvertParams p
       make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(c.x, c.y), pack_bf16x2(c.z, c.w));
 }
 
+// 128-wide accumulator interleaved by four query rows (dq_acc_index): one thread per
+// (batch, head, group of four queries, eight head-dim indices) reads 128 contiguous bytes
+// and writes eight bf16 of each of the four query rows.
+__global__ void __launch_bounds__(256) dq_convert4_kernel(const DqConvertParams p) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+  const int nqg = p.nqpad >> 2;
+  const int64_t total = static_cast<int64_t>(p.B) * p.Hq * nqg * 16;
+  if (t >= total) return;
+  const int c8 = static_cast<int>(t & 15) * 8;  // first head-dim index
+  const int64_t rest = t >> 4;
+  const int qg = static_cast<int>(rest % nqg);
+  const int64_t bh = rest / nqg;
+  const int h = static_cast<int>(bh % p.Hq);
+  const int b = static_cast<int>(bh / p.Hq);
+  if (c8 >= p.d) return;  // head-dim padding
+  const float4* src = reinterpret_cast<const float4*>(p.dq_acc + (bh * nqg + qg) * 512 + c8 * 4);
+  float v[8][4];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float4 x = src[e];
+    v[e][0] = x.x;
+    v[e][1] = x.y;
+    v[e][2] = x.z;
+    v[e][3] = x.w;
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int i = qg * 4 + r;
+    if (i >= p.Nq) break;
+    *reinterpret_cast<uint4*>(p.dq + ((static_cast<int64_t>(b) * p.Nq + i) * p.Hq + h) * p.d + c8) =
+        make_uint4(pack_bf16x2(v[0][r], v[1][r]), pack_bf16x2(v[2][r], v[3][r]), pack_bf16x2(v[4][r], v[5][r]),
+                   pack_bf16x2(v[6][r], v[7][r]));
+  }
+}
+
 // ----------------------------------------------------------------------- main backward
 enum BwdBar : int {
   kKVFull = 0,
@@ -137,19 +176,24 @@ enum BwdBar : int {
   kBEmpty = 10,
   kSFull = 11,
   kDpFull = 12,
-  kPReady = 13,
-  kDqFull = 14,
-  kDqFree = 15,
-  kDsFree = 16,
-  kFinal = 17,
-  kDrain = 18,
-  kNumBwdBars = 19
+  kPReady = 13,   // P^T of the step stored in TMEM (compute threads)
+  kDsReady = 14,  // dS^T of the step stored in shared memory, dP^T read (compute threads)
+  kDqFull = 15,
+  kDqFree = 16,   // dQ read out of TMEM (drain threads)
+  kDsFree = 17,
+  kFinal = 18,
+  kDrain = 19,
+  kNumBwdBars = 20
 };
 
-// 12 warps: warpgroup 0 = {TMA producer, MMA issuer, 2 idle}, warpgroups 1-2 = compute.
-constexpr int kBwdThreads = 384;
-constexpr uint32_t kRegsLow = 120, kRegsHigh = 192;
-constexpr int kBwdMinLaunchRegs = (kRegsLow + 2 * kRegsHigh) / 3;  // 168
+// 16 warps: warpgroup 0 = {TMA producer, MMA issuer, 2 idle}, warpgroups 1-2 = compute,
+// warpgroup 3 = dQ drain.  setmaxnreg moves registers from warpgroup 0 to the others; the
+// four shares add up to the 128 registers per thread the kernel is launched with.
+constexpr int kBwdThreads = 512;
+constexpr unsigned kDrainPaceNs = 32;  // pause after each 16-byte dQ reduction of a drain thread
+constexpr uint32_t kRegsCtl = 48, kRegsCompute = 160, kRegsDrain = 144;
+constexpr int kBwdMinLaunchRegs = (kRegsCtl + 2 * kRegsCompute + kRegsDrain) / 4;  // 128
+static_assert(kBwdMinLaunchRegs * kBwdThreads <= 65536, "register split exceeds the register file");
 
 // Shared memory: K, V resident; Q (+ lse, delta) in 2 slots; dO in 1 slot when a
 // bias tile needs the room, else 2; bias tile (one query tile, 32 KB); dS^T.
@@ -172,13 +216,15 @@ struct BwdSmem {
   static_assert(kTotal <= 232448, "bwd shared memory exceeds the per-CTA limit");
 };
 
-__device__ __forceinline__ uint64_t kmajor_step(int k, uint32_t rows) {
-  return static_cast<uint64_t>(((k >> 2) * rows * 128u + (k & 3) * 32u) >> 4);
+// Descriptor offsets (16-byte units) of the k-th 16-element K step of a 128-row SW128 tile
+// made of 64-column blocks: K-major (K along the 128-byte rows) and MN-major (K across rows).
+__host__ __device__ constexpr uint32_t kmajor_off(int k) {
+  return static_cast<uint32_t>(((k >> 2) * 128u * 128u + (k & 3) * 32u) >> 4);
 }
-__device__ __forceinline__ uint64_t mnmajor_step(int k) { return static_cast<uint64_t>((k * 2048) >> 4); }
+__host__ __device__ constexpr uint32_t mnmajor_off(int k) { return static_cast<uint32_t>((k * 2048) >> 4); }
 
 // The active query tiles of one key-tile column of the block map, from a shared-memory
-// copy packed 2 bits per query tile (kSkip / kPartial / kFull).
+// copy packed 2 bits per query tile (kSkip / kPartial / kFull), in increasing order.
 struct ColIter {
   const uint8_t* map2;
   int nTq;
@@ -189,11 +235,9 @@ struct ColIter {
     } while (qt < nTq && cls(qt) == kSkip);
     return qt;
   }
+  __device__ __forceinline__ int first() const { return next(-1); }
+  __device__ __forceinline__ bool valid(int qt) const { return qt < nTq; }
 };
-
-__device__ __forceinline__ void red_add_f32(float* gptr, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(gptr), "f"(v) : "memory");
-}
 
 // dO slot of step n (head hh of its query tile).  Without a bias there are two dO slots,
 // used alternately.  With a bias the second slot is the bias buffer (it directly follows the
@@ -215,7 +259,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr bool DQ_T = (D == 128);  // dQ^T = K^T dS^T (lane = head-dim index) for coalesced reductions
   constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);   // S^T, dP^T
   constexpr uint32_t IDESC_DV = idesc_bf16(128, D, false, true);     // P^T(tmem) x dO (N contiguous)
-  constexpr uint32_t IDESC_DK = idesc_bf16(128, D, false, true);     // dS^T(K-major) x Q (N contiguous)
+  constexpr uint32_t IDESC_DK = idesc_bf16(128, D, false, true);     // dS^T(tmem) x Q (N contiguous)
   constexpr uint32_t IDESC_DQ = DQ_T ? idesc_bf16(128, 128, true, true)   // K^T (M=d contiguous) x dS^T
                                      : idesc_bf16(128, D, true, true);    // dS (M contiguous) x K
 
@@ -252,7 +296,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBwdBars; ++i) mbar_init(&bars[i], 1);
     mbar_init(&bars[kPReady], 256);
-    mbar_init(&bars[kDqFree], 256);
+    mbar_init(&bars[kDsReady], 256);
+    mbar_init(&bars[kDqFree], 128);
     mbar_init(&bars[kBEmpty], 256);
     misc[1] = 0;
     fence_mbar_init();
@@ -273,11 +318,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = misc[0];
-  const int first_qt = it.next(-1);
-  const bool any_active = first_qt < p.nTq;
+  const int first_qt = it.first();
+  const bool any_active = it.valid(first_qt);
 
   if (warp < 4) {
-   regs_decrease<kRegsLow>();
+   regs_decrease<kRegsCtl>();
    if (warp == 0 && lane == 0 && any_active) {
     // ------------------------------------------------------------ producer
     tma_prefetch_desc(&tmQ);
@@ -304,7 +349,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ++nbias;
     };
     if (HAS_BIAS) load_bias(first_qt);  // the first bias tile has no predecessor in its buffer
-    for (int qt = first_qt; ok && qt < p.nTq; qt = it.next(qt), ++qi_count) {
+    for (int qt = first_qt; ok && it.valid(qt); qt = it.next(qt), ++qi_count) {
       for (int hh = 0; hh < p.G; ++hh, ++n) {
         const int h = g * p.G + hh;
         const int s = n & 1;
@@ -334,7 +379,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) break;
       if (HAS_BIAS) {
         const int nq = it.next(qt);
-        if (nq < p.nTq) {
+        if (it.valid(nq)) {
           // the next tile's bias goes into the buffer once its last dO there (or, with one head
           // per group, this tile's bias) has been released
           if (p.G >= 2) ok = mbar_wait(&bars[kDoEmpty + 1], (ufill1 - 1) & 1, p.err, kDevErrTimeout, abort_flag);
@@ -361,7 +406,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t kdesc_k = sdesc_sw128(smem_u32(sK), 16, 1024);
     const uint64_t vdesc_k = sdesc_sw128(smem_u32(sV), 16, 1024);
     const uint64_t kdesc_mn = sdesc_sw128(smem_u32(sK), 16384, 1024);
-    const uint64_t dsdesc_k = sdesc_sw128(smem_u32(sDS), 16, 1024);
     const uint64_t dsdesc_mn = sdesc_sw128(smem_u32(sDS), 16384, 1024);
     const uint64_t q0desc_k = sdesc_sw128(smem_u32(sQ), 16, 1024);
     const uint64_t q0desc_mn = sdesc_sw128(smem_u32(sQ), 16384, 1024);
@@ -370,68 +414,75 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t slot = static_cast<uint64_t>(L::kQB >> 4);
     int n = 0;
     int uuse0 = 0, uuse1 = 0;  // dO uses of slot 0 / slot 1
-    // S^T of step m (query slot m & 1); false after a failed wait
+    // S^T of step m (query slot m & 1) into columns 0..127; false after a failed wait
     auto issue_s = [&](int m) -> bool {
       const int s = m & 1;
       if (!mbar_wait(&bars[kQFull + s], (m >> 1) & 1, p.err, kDevErrTimeout, abort_flag)) return false;
       tc_fence_after();
       const uint64_t qdesc_k = q0desc_k + s * slot;
-      // S^T = K Q^T
-#pragma unroll
-      for (int k = 0; k < D / 16; ++k)
-        umma_ss(tbase, kdesc_k + kmajor_step(k, 128), qdesc_k + kmajor_step(k, 128), IDESC_S, k > 0);
+      static_for<0, D / 16>([&](auto kc) {
+        constexpr int k = decltype(kc)::value;
+        umma_ss_off<kmajor_off(k), kmajor_off(k)>(tbase, kdesc_k, qdesc_k, IDESC_S, k > 0);
+      });
       umma_commit(&bars[kSFull]);
       return true;
     };
-    // dP^T of step m (dO slot sd), into the columns the previous dQ used
+    // dP^T of step m (dO slot sd) into columns 128..255, which the previous dQ used
     auto issue_dp = [&](int m, int sd) -> bool {
       const uint64_t dodesc_k = do0desc_k + sd * slot;
       if (!mbar_wait(&bars[kDoFull + sd], (sd ? uuse1 : uuse0) & 1, p.err, kDevErrTimeout, abort_flag)) return false;
       if (m > 0 && !mbar_wait(&bars[kDqFree], (m - 1) & 1, p.err, kDevErrTimeout, abort_flag)) return false;
       tc_fence_after();
-#pragma unroll
-      for (int k = 0; k < D / 16; ++k)
-        umma_ss(tbase + 128, vdesc_k + kmajor_step(k, 128), dodesc_k + kmajor_step(k, 128), IDESC_S, k > 0);
+      static_for<0, D / 16>([&](auto kc) {
+        constexpr int k = decltype(kc)::value;
+        umma_ss_off<kmajor_off(k), kmajor_off(k)>(tbase + 128, vdesc_k, dodesc_k, IDESC_S, k > 0);
+      });
       umma_commit(&bars[kDpFull]);
       return true;
     };
-    // Per step n: dQ(n), dV(n), S^T(n+1), dK(n), dP^T(n+1).  S^T(n+1) needs only dV(n) to have
-    // read P^T(n) and dP^T(n+1) only the drain of dQ(n), which dK(n) overlaps; the next step's
-    // inputs are then ready while this step's dQ is still being reduced.
+    // Per step n: dV(n) as soon as P^T(n) is stored (it overlaps the dS pass), then, once
+    // dS^T(n) is stored, S^T(n+1), dK(n), dQ(n), dP^T(n+1).  The compute warps start on
+    // P^T(n+1) as soon as S^T(n+1) is done.  dK(n) reads dS^T(n) from TMEM (packed by the dS
+    // pass into the dP^T columns it has read) before dQ(n) overwrites those columns, and it
+    // frees the Q slot early for the load two steps ahead; the drain warps read dQ(n) out of
+    // TMEM before dP^T(n+1) needs its columns.
     ok = ok && issue_s(0) && issue_dp(0, do_slot<HAS_BIAS>(0, 0, p.G));
-    for (int qt = first_qt; ok && qt < p.nTq; qt = it.next(qt)) {
+    for (int qt = first_qt; ok && it.valid(qt); qt = it.next(qt)) {
       for (int hh = 0; hh < p.G; ++hh, ++n) {
         const int s = n & 1, sd = do_slot<HAS_BIAS>(n, hh, p.G);
         const uint64_t qdesc_mn = q0desc_mn + s * slot, dodesc_mn = do0desc_mn + sd * slot;
         if (!(ok = mbar_wait(&bars[kPReady], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
         tc_fence_after();
-        // dQ first (K dimension = 128 keys; written over the dP^T columns, which the compute
-        // warps have read): its drain then overlaps the products below
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (DQ_T)
-            umma_ss(tbase + 128, kdesc_mn + mnmajor_step(k), dsdesc_mn + mnmajor_step(k), IDESC_DQ, k > 0);
-          else
-            umma_ss(tbase + 128, dsdesc_mn + mnmajor_step(k), kdesc_mn + mnmajor_step(k), IDESC_DQ, k > 0);
-        }
-        umma_commit(&bars[kDqFull]);
         // dV += P^T dO  (K dimension = 128 queries; P^T packed in TMEM cols 0..31 and 64..95)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          umma_ts(tbase + 256, tbase + k * 8 + (k >= 4 ? 32 : 0), dodesc_mn + mnmajor_step(k), IDESC_DV,
-                  (n > 0 || k > 0) ? 1u : 0u);
-        umma_commit(&bars[kDoEmpty + sd]);
+        static_for<0, 8>([&](auto kc) {
+          constexpr int k = decltype(kc)::value;
+          umma_ts_off<k * 8 + (k >= 4 ? 32 : 0), mnmajor_off(k)>(tbase + 256, tbase, dodesc_mn, IDESC_DV,
+                                                                  (n > 0 || k > 0) ? 1u : 0u);
+        });
+        umma_commit(&bars[kDoEmpty + sd]);  // dP^T(n) and dV(n) have read this dO slot
         if (sd) ++uuse1;
         else ++uuse0;
-        const bool more = hh + 1 < p.G || it.next(qt) < p.nTq;
-        if (more && !(ok = issue_s(n + 1))) break;
-        // dK += dS^T Q
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          umma_ss(tbase + 384, dsdesc_k + kmajor_step(k, 128), qdesc_mn + mnmajor_step(k), IDESC_DK,
-                  (n > 0 || k > 0) ? 1u : 0u);
+        if (!(ok = mbar_wait(&bars[kDsReady], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        tc_fence_after();
+        const bool more = hh + 1 < p.G || it.valid(it.next(qt));
+        if (more && !(ok = issue_s(n + 1))) break;  // over P^T(n), which dV(n) and the dS pass have read
+        // dK += dS^T Q  (TS: dS^T packed in TMEM cols 128..159 and 192..223)
+        static_for<0, 8>([&](auto kc) {
+          constexpr int k = decltype(kc)::value;
+          umma_ts_off<128 + k * 8 + (k >= 4 ? 32 : 0), mnmajor_off(k)>(tbase + 384, tbase, qdesc_mn, IDESC_DK,
+                                                                        (n > 0 || k > 0) ? 1u : 0u);
+        });
         umma_commit(&bars[kQEmpty + s]);
-        umma_commit(&bars[kDsFree]);
+        // dQ (K dimension = 128 keys) over the dP^T columns, after dK has read dS^T there
+        static_for<0, 8>([&](auto kc) {
+          constexpr int k = decltype(kc)::value;
+          if (DQ_T)
+            umma_ss_off<mnmajor_off(k), mnmajor_off(k)>(tbase + 128, kdesc_mn, dsdesc_mn, IDESC_DQ, k > 0);
+          else
+            umma_ss_off<mnmajor_off(k), mnmajor_off(k)>(tbase + 128, dsdesc_mn, kdesc_mn, IDESC_DQ, k > 0);
+        });
+        umma_commit(&bars[kDqFull]);
+        umma_commit(&bars[kDsFree]);  // the shared-memory dS^T tile has been read
         if (more) {
           const int hn = hh + 1 < p.G ? hh + 1 : 0;
           if (!(ok = issue_dp(n + 1, do_slot<HAS_BIAS>(n + 1, hn, p.G)))) break;
@@ -442,13 +493,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     umma_commit(&bars[kDrain]);
     mbar_wait(&bars[kDrain], 0, p.err, kDevErrTimeout, nullptr);
    }
-  } else {
-   regs_increase<kRegsHigh>();
+  } else if (warp < 12) {
+   regs_increase<kRegsCompute>();
    {
     // ------------------------------------------------------------ compute
     // Two warpgroups: wg 0 owns queries 0..63 of every step, wg 1 queries 64..127.
-    // Thread (quad, lane) owns key row j of S^T/dP^T/dK/dV, and row j of the dQ
-    // accumulator in TMEM (head-dim index j for d = 128, query row j for d = 64).
+    // Thread (quad, lane) owns key row j of S^T/dP^T/dK/dV.  Per step: the P pass (S^T ->
+    // P^T, packed bf16 into this warpgroup's own S^T columns), then the dS pass (P^T and
+    // dP^T -> scale * dS^T into shared memory, dBias partial sums in registers).
     const int wg = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int j = quad * 32 + lane;
@@ -457,18 +509,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool kin = kidx < p.Nk;
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
     const int qbase = wg * 64;
-    uint64_t acc2[WANT_DBIAS ? 32 : 1];  // dBias partial sums, pairs of queries
+    uint64_t acc2[WANT_DBIAS ? 32 : 1];  // dBias partial sums (of scale * dS), pairs of queries
 #pragma unroll
     for (int c = 0; c < (WANT_DBIAS ? 32 : 1); ++c) acc2[c] = 0ull;
     const uint64_t sc2 = f2(p.scale_log2, p.scale_log2);
+    const uint64_t scl2 = f2(p.scale, p.scale);
     const uint64_t lg2 = f2(kLog2e, kLog2e);
     int n = 0, qi_count = 0;
     bool ok = true;
     // No compute thread leaves these loops early, so every one of them reaches every named
     // barrier below; after a failed wait (ok == false) the work and the stores are skipped.
     // Per query tile: the keep bits of queries qbase..qbase+63 for key j and the bias^T column
-    // slice, copied once into registers for every head.  The next tile's are fetched while
-    // the last head of the current tile waits for its dQ product.
+    // slice, copied once into registers for every head.  The next tile's are fetched right
+    // after the P pass of the current tile's last head, the only pass that uses them.
     uint32_t bw0 = ~0u, bw1 = ~0u;
     uint32_t bpk[HAS_BIAS ? 32 : 1];
     auto fetch_tile = [&](int qt, int qi) {
@@ -498,139 +551,153 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(&bars[kBEmpty]);
       }
     };
-    if (first_qt < p.nTq) fetch_tile(first_qt, 0);
-    for (int qt = first_qt; qt < p.nTq; qt = it.next(qt), ++qi_count) {
+    // Once the steps that read the dS^T tile are done (kDsFree), stage the summed dBias of the
+    // query tile at q0t in it as a (query, key) SW128 tile and TMA-store it; the caller waits
+    // for the store's read before the tile is written again.
+    auto stage_dbias = [&](int q0t) {
+      uint8_t* dbt = sDS + (j >> 6) * 16384 + (j & 7) * 2;
+      const int jc = (j & 63) >> 3;
+      const uint64_t inv2 = f2(1.f / p.scale, 1.f / p.scale);  // the sums are of scale * dS
+#pragma unroll
+      for (int qp = 0; qp < 32; ++qp) {
+        const int i = qbase + 2 * qp;
+        float a0, a1;
+        f2split(mul2(acc2[qp], inv2), a0, a1);
+        const uint32_t w = pack_bf16x2(a0, a1);
+        if (ok) {
+          *reinterpret_cast<uint16_t*>(dbt + i * 128 + ((jc ^ (i & 7)) << 4)) = static_cast<uint16_t>(w & 0xFFFFu);
+          *reinterpret_cast<uint16_t*>(dbt + (i + 1) * 128 + ((jc ^ ((i + 1) & 7)) << 4)) =
+              static_cast<uint16_t>(w >> 16);
+        }
+        acc2[qp] = 0ull;
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 256);
+      if (ctid == 0 && ok) {
+        const uint64_t pol = l2_evict_first();  // dBias is written once, never read here
+        tma_store_4d_hint(&tmDB, sDS, k0, q0t, g, b, pol);
+        tma_store_4d_hint(&tmDB, sDS + 16384, k0 + 64, q0t, g, b, pol);
+        bulk_commit_group();
+      }
+    };
+    if (any_active) fetch_tile(first_qt, 0);
+    int q0_prev = 0;
+    for (int qt = first_qt; it.valid(qt); qt = it.next(qt), ++qi_count) {
       const int q0 = qt * kTile;
-      const int rows_in = min(kTile, p.Nq - q0) - qbase;  // valid queries in this half
       for (int hh = 0; hh < p.G; ++hh, ++n) {
-        const int h = g * p.G + hh;
         const int s = n & 1;
+        // ---------------- P pass: P^T = exp2(S^T * scale*log2e + bias^T*log2e - lse*log2e)
         ok = ok && mbar_wait(&bars[kSFull], n & 1, p.err, kDevErrTimeout, abort_flag);
-        ok = ok && mbar_wait(&bars[kDpFull], n & 1, p.err, kDevErrTimeout, abort_flag);
         ok = ok && mbar_wait(&bars[kQFull + s], (n >> 1) & 1, p.err, kDevErrTimeout, abort_flag);
-        ok = ok && (n == 0 || mbar_wait(&bars[kDsFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag));
+        if (ok) {
+          tc_fence_after();
+          const float* lse2 = sLse + s * 128 + qbase;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {  // 16 queries per chunk
+            const int col = qbase + c * 16;
+            uint32_t sr[16];
+            tmem_ld16(tl + col, sr);
+            uint64_t nl[8];  // this chunk's 16 -lse*log2(e) values as pairs (broadcast 16-byte reads)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const ulonglong2 a = reinterpret_cast<const ulonglong2*>(lse2 + c * 16)[v];
+              nl[2 * v] = a.x;
+              nl[2 * v + 1] = a.y;
+            }
+            tmem_ld_wait();
+            const uint32_t word = c < 2 ? bw0 : bw1;
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              const int qi = c * 16 + e;  // 0..63 within this half (even)
+              const uint64_t s2 = f2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+              const uint64_t x2 = HAS_BIAS ? fma2(s2, sc2, fma2(bf16x2_to_f2(bpk[qi >> 1]), lg2, nl[e >> 1]))
+                                           : fma2(s2, sc2, nl[e >> 1]);
+              float x0, x1;
+              f2split(x2, x0, x1);
+              // with a bias the keep bits are already folded into it as -inf
+              const float p0 = (HAS_BIAS || ((word >> (qi & 31)) & 1u)) ? ex2(x0) : 0.f;
+              const float p1 = (HAS_BIAS || ((word >> ((qi + 1) & 31)) & 1u)) ? ex2(x1) : 0.f;
+              pk[e >> 1] = pack_bf16x2(p0, p1);
+            }
+            // packed P^T stays inside this warpgroup's own S^T columns (already read):
+            // queries 0..63 -> cols 0..31, queries 64..127 -> cols 64..95
+            tmem_st8(tl + wg * 64 + c * 8, pk);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&bars[kPReady]);
+        }
+        if (hh == p.G - 1) {  // the bits and bias^T slice of this tile are no longer needed
+          const int nq = it.next(qt);
+          if (it.valid(nq)) fetch_tile(nq, qi_count + 1);
+        }
+        // ---------------- dS pass: scale * dS^T = P^T (scale * dP^T - scale * delta)
+        ok = ok && mbar_wait(&bars[kDpFull], n & 1, p.err, kDevErrTimeout, abort_flag);
         if (WANT_DBIAS && hh == 0 && qi_count > 0) {
-          // the previous tile's dBias store must have read the dS^T tile before it is rewritten
+          // the previous query tile's dBias goes out through the dS^T tile first, once the
+          // previous step's dQ and dK products have read that tile
+          ok = ok && mbar_wait(&bars[kDsFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag);
+          stage_dbias(q0_prev);
           if (ctid == 0) bulk_wait_read_all();
           named_bar_sync(1, 256);
         }
-        if (!ok) continue;
-        tc_fence_after();
-        const float* lse2 = sLse + s * 128 + qbase;
-        const float* dlt = sDelta + s * 128 + qbase;
+        if (ok) {
+          tc_fence_after();
+          const float* dlt = sDelta + s * 128 + qbase;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {  // 16 queries per chunk
-          const int col = qbase + c * 16;
-          uint32_t sr[16], dr[16];
-          tmem_ld16(tl + col, sr);
-          tmem_ld16(tl + 128 + col, dr);
-          uint64_t nl[8], dd[8];  // this chunk's 16 -lse2 / delta values as pairs (broadcast 16-byte reads)
+          for (int c = 0; c < 4; ++c) {
+            const int col = qbase + c * 16;
+            uint32_t pp[8], dr[16];
+            tmem_ld8(tl + wg * 64 + c * 8, pp);
+            tmem_ld16(tl + 128 + col, dr);
+            uint64_t dd[8];  // this chunk's 16 -scale*delta values as pairs
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const ulonglong2 a = reinterpret_cast<const ulonglong2*>(lse2 + c * 16)[v];
-            const ulonglong2 bq = reinterpret_cast<const ulonglong2*>(dlt + c * 16)[v];
-            nl[2 * v] = a.x; nl[2 * v + 1] = a.y;
-            dd[2 * v] = bq.x; dd[2 * v + 1] = bq.y;
+            for (int v = 0; v < 4; ++v) {
+              const ulonglong2 bq = reinterpret_cast<const ulonglong2*>(dlt + c * 16)[v];
+              dd[2 * v] = bq.x;
+              dd[2 * v + 1] = bq.y;
+            }
+            tmem_ld_wait();
+            uint32_t dk[8];
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              const int qi = c * 16 + e;
+              // scale * dS = P * (scale * dP - scale * delta): the scale of dQ and dK is applied here
+              const uint64_t dv2 = mul2(bf16x2_to_f2(pp[e >> 1]),
+                                        fma2(f2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), scl2, dd[e >> 1]));
+              if (WANT_DBIAS) acc2[qi >> 1] = add2(acc2[qi >> 1], dv2);
+              float d0, d1;
+              f2split(dv2, d0, d1);
+              dk[e >> 1] = pack_bf16x2(d0, d1);
+            }
+            // packed dS^T for the dK product, in this warpgroup's dP^T columns already read:
+            // queries 0..63 -> cols 128..159, queries 64..127 -> cols 192..223
+            tmem_st8(tl + 128 + wg * 64 + c * 8, dk);
+            // the previous step's dQ must have read the shared-memory dS^T tile
+            if (c == 0 && n > 0 && !mbar_wait(&bars[kDsFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag)) {
+              ok = false;
+              break;
+            }
+            // dS^T row j, queries col..col+15: two 16-byte chunks of the SW128 K-major tile
+            uint8_t* rowp = sDS + wg * 16384 + j * 128;
+            *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (j & 7)) << 4)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
+            *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (j & 7)) << 4)) = make_uint4(dk[4], dk[5], dk[6], dk[7]);
           }
-          tmem_ld_wait();
-          const uint32_t word = c < 2 ? bw0 : bw1;
-          uint32_t pk[8], dk[8];
-#pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            const int qi = c * 16 + e;  // 0..63 within this half (even)
-            const uint64_t s2 = f2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
-            const uint64_t x2 = HAS_BIAS ? fma2(s2, sc2, fma2(bf16x2_to_f2(bpk[qi >> 1]), lg2, nl[e >> 1]))
-                                         : fma2(s2, sc2, nl[e >> 1]);
-            float x0, x1;
-            f2split(x2, x0, x1);
-            // with a bias the keep bits are already folded into it as -inf
-            const float p0 = (HAS_BIAS || ((word >> (qi & 31)) & 1u)) ? ex2(x0) : 0.f;
-            const float p1 = (HAS_BIAS || ((word >> ((qi + 1) & 31)) & 1u)) ? ex2(x1) : 0.f;
-            const uint64_t dv2 =
-                mul2(f2(p0, p1), sub2(f2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), dd[e >> 1]));
-            if (WANT_DBIAS) acc2[qi >> 1] = add2(acc2[qi >> 1], dv2);
-            float d0, d1;
-            f2split(dv2, d0, d1);
-            pk[e >> 1] = pack_bf16x2(p0, p1);
-            dk[e >> 1] = pack_bf16x2(d0, d1);
-          }
-          // packed P^T stays inside this warpgroup's own S^T columns (already read):
-          // queries 0..63 -> cols 0..31, queries 64..127 -> cols 64..95
-          tmem_st8(tl + wg * 64 + c * 8, pk);
-          // dS^T row j, queries col..col+15: two 16-byte chunks of the SW128 K-major tile
-          uint8_t* rowp = sDS + wg * 16384 + j * 128;
-          *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (j & 7)) << 4)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
-          *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (j & 7)) << 4)) = make_uint4(dk[4], dk[5], dk[6], dk[7]);
-        }
-        fence_proxy_async_smem();
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&bars[kPReady]);
-        if (hh == p.G - 1) {  // the bits and bias^T slice of this tile are no longer needed
-          const int nq = it.next(qt);
-          if (nq < p.nTq) fetch_tile(nq, qi_count + 1);
-        }
-        // drain dQ into the fp32 accumulator
-        if (!(ok = mbar_wait(&bars[kDqFull], n & 1, p.err, kDevErrTimeout, abort_flag))) continue;
-        tc_fence_after();
-        // Both 32-column pieces are read before the columns are released, so the next
-        // step's dP^T product can start while the reductions below are still issuing.
-        // (d = 64: this warpgroup's 32 head-dim columns are one piece)
-        uint32_t r0[32], r1[32];
-        tmem_ld32(tl + 128 + (DQ_T ? qbase : wg * (D / 2)), r0);
-        if (DQ_T) tmem_ld32(tl + 128 + qbase + 32, r1);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&bars[kDqFree]);
-        if (DQ_T) {
-          // lane = head-dim index j, columns = this warpgroup's 64 queries: each warp
-          // instruction adds 32 consecutive floats of one query row
-          const int64_t rstride = static_cast<int64_t>(p.Hq) * D;
-          float* dst = p.dq_acc + ((static_cast<int64_t>(b) * p.nqpad + q0 + qbase) * p.Hq + h) * D + j;
-          if (j < p.d) {  // head-dim rows past d are padding (zero)
-#pragma unroll
-            for (int t = 0; t < 32; ++t, dst += rstride) red_add_f32(dst, __uint_as_float(r0[t]) * p.scale);
-#pragma unroll
-            for (int t = 0; t < 32; ++t, dst += rstride) red_add_f32(dst, __uint_as_float(r1[t]) * p.scale);
-          }
-        } else {
-          float* dqrow = p.dq_acc + ((static_cast<int64_t>(b) * p.nqpad + q0 + j) * p.Hq + h) * D + wg * (D / 2);
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            if (wg * (D / 2) + 4 * v < p.d)
-              red_add_v4(dqrow + 4 * v, __uint_as_float(r0[4 * v]) * p.scale,
-                         __uint_as_float(r0[4 * v + 1]) * p.scale, __uint_as_float(r0[4 * v + 2]) * p.scale,
-                         __uint_as_float(r0[4 * v + 3]) * p.scale);
-        }
-      }
-      if (WANT_DBIAS) {
-        // Once the last head's dQ / dK products are done with the dS^T tile, stage this
-        // query tile's dBias in it as a (query, key) SW128 tile and TMA-store it.
-        ok = ok && mbar_wait(&bars[kDsFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag);
-        uint8_t* dbt = sDS + (j >> 6) * 16384 + (j & 7) * 2;
-        const int jc = (j & 63) >> 3;
-#pragma unroll
-        for (int qp = 0; qp < 32; ++qp) {
-          const int i = qbase + 2 * qp;
-          float a0, a1;
-          f2split(acc2[qp], a0, a1);
-          const uint32_t w = pack_bf16x2(a0, a1);
           if (ok) {
-            *reinterpret_cast<uint16_t*>(dbt + i * 128 + ((jc ^ (i & 7)) << 4)) = static_cast<uint16_t>(w & 0xFFFFu);
-            *reinterpret_cast<uint16_t*>(dbt + (i + 1) * 128 + ((jc ^ ((i + 1) & 7)) << 4)) =
-                static_cast<uint16_t>(w >> 16);
+            fence_proxy_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bars[kDsReady]);
           }
-          acc2[qp] = 0ull;
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, 256);
-        if (ctid == 0 && ok) {
-          const uint64_t pol = l2_evict_first();  // dBias is written once, never read here
-          tma_store_4d_hint(&tmDB, sDS, k0, q0, g, b, pol);
-          tma_store_4d_hint(&tmDB, sDS + 16384, k0 + 64, q0, g, b, pol);
-          bulk_commit_group();
         }
       }
+      q0_prev = q0;
+    }
+    if (WANT_DBIAS && n > 0) {
+      // the last query tile's dBias, once its last step's products are done with dS^T
+      ok = ok && mbar_wait(&bars[kDsFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag);
+      stage_dbias(q0_prev);
     }
     if (ok && n > 0) ok = mbar_wait(&bars[kFinal], 0, p.err, kDevErrTimeout, abort_flag);
     // zero-fill the dBias tiles of this key column that were skipped (TMA stores of a zero tile)
@@ -654,13 +721,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       named_bar_sync(1, 256);
     }
-    // dK (warpgroup 0) and dV (warpgroup 1)
+    // dK (warpgroup 0) and dV (warpgroup 1); both accumulators already carry their scale
     if (ok) {
       tc_fence_after();
       const int64_t off = ((static_cast<int64_t>(b) * p.Nk + kidx) * p.Hkv + g) * p.d;
       uint16_t* dst = (wg == 0 ? p.dk : p.dv) + off;
       const uint32_t col0 = wg == 0 ? 384u : 256u;
-      const float sc = wg == 0 ? p.scale : 1.f;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
@@ -673,13 +739,86 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         uint32_t pk[16];
 #pragma unroll
-        for (int t = 0; t < 16; ++t)
-          pk[t] = pack_bf16x2(__uint_as_float(r[2 * t]) * sc, __uint_as_float(r[2 * t + 1]) * sc);
+        for (int t = 0; t < 16; ++t) pk[t] = pack_bf16x2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1]));
         if (kin) {  // columns past the head dim are padding
           uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
           for (int v = 0; v < 4; ++v)
             if (c * 32 + v * 8 < p.d) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+    }
+   }
+  } else {
+   regs_increase<kRegsDrain>();
+   if (any_active) {
+    // ------------------------------------------------------------ dQ drain
+    // Warp (12 + quad) reads TMEM lanes quad*32..+31 of the dQ product of every step (d = 128:
+    // lane = head-dim index, columns = the 128 queries; d = 64: lane = query, columns = head
+    // dim), releases the columns for the next dP^T and adds the values to the fp32 accumulator.
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
+    int n = 0;
+    bool ok = true;
+    for (int qt = first_qt; ok && it.valid(qt); qt = it.next(qt)) {
+      const int q0 = qt * kTile;
+      for (int hh = 0; hh < p.G; ++hh, ++n) {
+        const int h = g * p.G + hh;
+        if (!(ok = mbar_wait(&bars[kDqFull], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        tc_fence_after();
+        if (DQ_T) {
+          uint32_t r0[32], r1[32], r2[32], r3[32];
+          tmem_ld32(tl + 128, r0);
+          tmem_ld32(tl + 160, r1);
+          tmem_ld32(tl + 192, r2);
+          tmem_ld32(tl + 224, r3);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&bars[kDqFree]);
+          // The accumulator is interleaved by four queries (dq_acc_index), so each thread adds
+          // four queries with one 16-byte reduction and a warp instruction covers 512
+          // contiguous bytes.  The reductions are paced (kDrainPaceNs after each) so that they
+          // leave the SM about as fast as the memory system accepts them: a backlog of
+          // reductions stalls the other warps' shared-memory and TMEM accesses and the tensor
+          // core's operand reads.
+          if (row < p.d) {  // head-dim rows past d are padding (zero)
+            float* dst = p.dq_acc + dq_acc_index(b, h, q0, row, p.Hq, p.nqpad, 128);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              red_add_v4(dst + u * 512, __uint_as_float(r0[4 * u]), __uint_as_float(r0[4 * u + 1]),
+                         __uint_as_float(r0[4 * u + 2]), __uint_as_float(r0[4 * u + 3])), __nanosleep(kDrainPaceNs);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              red_add_v4(dst + (8 + u) * 512, __uint_as_float(r1[4 * u]), __uint_as_float(r1[4 * u + 1]),
+                         __uint_as_float(r1[4 * u + 2]), __uint_as_float(r1[4 * u + 3])), __nanosleep(kDrainPaceNs);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              red_add_v4(dst + (16 + u) * 512, __uint_as_float(r2[4 * u]), __uint_as_float(r2[4 * u + 1]),
+                         __uint_as_float(r2[4 * u + 2]), __uint_as_float(r2[4 * u + 3])), __nanosleep(kDrainPaceNs);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              red_add_v4(dst + (24 + u) * 512, __uint_as_float(r3[4 * u]), __uint_as_float(r3[4 * u + 1]),
+                         __uint_as_float(r3[4 * u + 2]), __uint_as_float(r3[4 * u + 3])), __nanosleep(kDrainPaceNs);
+          }
+        } else {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tl + 128, r0);
+          tmem_ld32(tl + 160, r1);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&bars[kDqFree]);
+          float* dqrow = p.dq_acc + dq_acc_index(b, h, q0 + row, 0, p.Hq, p.nqpad, D);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            if (4 * v < p.d)
+              red_add_v4(dqrow + 4 * v, __uint_as_float(r0[4 * v]), __uint_as_float(r0[4 * v + 1]),
+                         __uint_as_float(r0[4 * v + 2]), __uint_as_float(r0[4 * v + 3]));
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            if (32 + 4 * v < p.d)
+              red_add_v4(dqrow + 32 + 4 * v, __uint_as_float(r1[4 * v]), __uint_as_float(r1[4 * v + 1]),
+                         __uint_as_float(r1[4 * v + 2]), __uint_as_float(r1[4 * v + 3]));
         }
       }
     }
@@ -721,6 +860,12 @@ cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_dq_convert(const DqConvertParams& p, cudaStream_t stream) {
+  if (p.dpad == 128) {
+    const int64_t total = static_cast<int64_t>(p.B) * p.Hq * (p.nqpad / 4) * 16;
+    if (total == 0) return cudaSuccess;
+    dq_convert4_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
   const int64_t total = static_cast<int64_t>(p.B) * p.Nq * p.Hq * p.d / 8;
   if (total == 0) return cudaSuccess;
   dq_convert_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(p);

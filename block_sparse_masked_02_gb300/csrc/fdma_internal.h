@@ -60,14 +60,26 @@ struct FwdParams {
 
 struct BwdPreParams {
   int B, Nq, Hq, d, nqpad;
-  int dpad;  // row width of the dQ accumulator (64 or 128)
+  int dpad;     // row width of the dQ accumulator (64 or 128)
+  float scale;  // softmax scale
   const uint16_t* out;
   const uint16_t* dout;
   const float* lse;
   float* lse2;   // (B,Hq,nqpad): -lse*log2(e), -inf for empty / padded rows
-  float* delta;  // (B,Hq,nqpad)
-  float* dq_acc; // (B,nqpad,Hq,d), zeroed
+  float* delta;  // (B,Hq,nqpad): -scale * <dO_i, O_i>
+  float* dq_acc; // dQ accumulator (layout: dq_acc_index), zeroed
 };
+
+// fp32 dQ accumulator of the backward.  For the 128-wide kernels it is interleaved by
+// groups of four query rows, (B, Hq, nqpad/4, 128, 4): element (query i, head-dim c) of a
+// head sits at ((i/4)*128 + c)*4 + i%4, so the four queries of one head-dim index are one
+// 16-byte vector and 32 consecutive head-dim indices are 512 contiguous bytes.  For the
+// 64-wide kernels it is (B, nqpad, Hq, 64).
+__host__ __device__ inline int64_t dq_acc_index(int b, int h, int i, int c, int Hq, int nqpad, int dpad) {
+  if (dpad == 128)
+    return (((static_cast<int64_t>(b) * Hq + h) * (nqpad >> 2) + (i >> 2)) * 128 + c) * 4 + (i & 3);
+  return ((static_cast<int64_t>(b) * nqpad + i) * Hq + h) * dpad + c;
+}
 
 struct BwdParams {
   int B, Nq, Nk, Hq, Hkv, G, nTq, nTk, nqpad;
