@@ -250,6 +250,7 @@ int fdma_fwd(const fdma_args* a, void* out, float* lse, void* stream_v) {
   p.nTk = cdiv(a->Nk, kTile);
   p.scale = a->scale;
   p.scale_log2 = a->scale * 1.4426950408889634f;
+  p.test_short_wait = (a->flags & FDMA_FLAG_TEST_SHORT_WAIT) ? 1 : 0;
   p.bias_bsel = a->bias_stride[0] == 0 ? 0 : 1;
   p.bias_hsel = a->bias_stride[1] == 0 ? 0 : 1;
   p.kmap = reinterpret_cast<const int8_t*>(ws + w.kmap);
@@ -321,6 +322,7 @@ int fdma_bwd(const fdma_args* a, const void* out, const void* dout, const float*
   p.nqpad = nqpad;
   p.scale = a->scale;
   p.scale_log2 = a->scale * 1.4426950408889634f;
+  p.test_short_wait = (a->flags & FDMA_FLAG_TEST_SHORT_WAIT) ? 1 : 0;
   p.kmap = reinterpret_cast<const int8_t*>(ws + w.kmap);
   p.bits_col = reinterpret_cast<const uint4*>(ws + w.bits_col);
   p.bias = static_cast<const uint16_t*>(a->bias);

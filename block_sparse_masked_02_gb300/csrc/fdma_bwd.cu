@@ -183,7 +183,8 @@ enum BwdBar : int {
   kDsFree = 17,
   kFinal = 18,
   kDrain = 19,
-  kNumBwdBars = 20
+  kNever = 20,    // never arrived at: the target of the test wait (FDMA_FLAG_TEST_SHORT_WAIT)
+  kNumBwdBars = 21
 };
 
 // 16 warps: warpgroup 0 = {TMA producer, MMA issuer, 2 idle}, warpgroups 1-2 = compute,
@@ -337,7 +338,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_load_4d(sK + c * 16384, &tmK, &bars[kKVFull], c * 64, k0, g, b);
       tma_load_4d(sV + c * 16384, &tmV, &bars[kKVFull], c * 64, k0, g, b);
     }
-    int n = 0, qi_count = 0, nbias = 0;
+    int n = 0, qi_count = 0, nbias = 0, nq_issued = 0;
     int ufill0 = 0, ufill1 = 0;  // dO fills of slot 0 / slot 1
     bool ok = true;
     auto load_bias = [&](int qt) {
@@ -361,6 +362,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int64_t vec = (static_cast<int64_t>(b) * p.Hq + h) * p.nqpad + qt * kTile;
         bulk_load(sLse + s * 128, p.lse2 + vec, 512, &bars[kQFull + s]);
         bulk_load(sDelta + s * 128, p.delta + vec, 512, &bars[kQFull + s]);
+        nq_issued = n + 1;
         const int sd = do_slot<HAS_BIAS>(n, hh, p.G);
         const int u = sd ? ufill1 : ufill0;
         if (HAS_BIAS && sd == 1 && hh == (((p.G - 1) & 1) ? 0 : 1)) {
@@ -392,7 +394,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (*abort_flag) {
       // let this CTA's own copies land before it retires (bounded waits)
       mbar_wait(&bars[kKVFull], 0, p.err, kDevErrTimeout, nullptr);
-      for (int m = n > 2 ? n - 2 : 0; m <= n; ++m)
+      for (int m = nq_issued > 2 ? nq_issued - 2 : 0; m < nq_issued; ++m)
         mbar_wait(&bars[kQFull + (m & 1)], (m >> 1) & 1, p.err, kDevErrTimeout, nullptr);
       // only the last fill of each slot can still be in flight
       if (ufill0 > 0) mbar_wait(&bars[kDoFull + 0], (ufill0 - 1) & 1, p.err, kDevErrTimeout, nullptr);
@@ -516,7 +518,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t scl2 = f2(p.scale, p.scale);
     const uint64_t lg2 = f2(kLog2e, kLog2e);
     int n = 0, qi_count = 0;
-    bool ok = true;
+    // With FDMA_FLAG_TEST_SHORT_WAIT every compute thread first waits on a barrier that
+    // nothing arrives at, with a short limit: the wait expires, records FDMA_ERR_TIMEOUT and
+    // raises the abort flag, and the CTA unwinds as after any expired wait.
+    bool ok = !p.test_short_wait ||
+              mbar_wait(&bars[kNever], 0, p.err, kDevErrTimeout, abort_flag, kTestWaitNs);
     // No compute thread leaves these loops early, so every one of them reaches every named
     // barrier below; after a failed wait (ok == false) the work and the stores are skipped.
     // Per query tile: the keep bits of queries qbase..qbase+63 for key j and the bias^T column

@@ -47,7 +47,8 @@ enum FwdBar : int {
   kODone = 17,
   kOFinal = 18,
   kDrain = 19,
-  kNumFwdBars = 20
+  kFNever = 20,  // never arrived at: the target of the test wait (FDMA_FLAG_TEST_SHORT_WAIT)
+  kNumFwdBars = 21
 };
 
 template <int D, bool HAS_BIAS>
@@ -246,9 +247,11 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
     float m_ref = kNegInf, l = 0.f;
     int n = 0;
-    bool ok = true;
+    // FDMA_FLAG_TEST_SHORT_WAIT: a wait on a barrier nothing arrives at expires first
+    bool ok = !p.test_short_wait ||
+              mbar_wait(&bars[kFNever], 0, p.err, kDevErrTimeout, abort_flag, kTestWaitNs);
     uint32_t raw[32];
-    for (int kt = first_kt; kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
+    for (int kt = first_kt; ok && kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
       const int s = n & 1;
       const uint32_t ph = (n >> 1) & 1;
       if (!(ok = mbar_wait(&bars[kSFull + s], ph, p.err, kDevErrTimeout, abort_flag))) break;
@@ -410,7 +413,8 @@ enum Fwd2Bar : int {
   k2PReady = 13,   // +2*head+half (4): P of keys 0..63 / 64..127 stored
   k2OFinal = 17,
   k2Drain = 18,
-  kNumFwd2Bars = 19
+  k2Never = 19,  // never arrived at: the target of the test wait (FDMA_FLAG_TEST_SHORT_WAIT)
+  kNumFwd2Bars = 20
 };
 
 constexpr int kFwd2Threads = 384;
@@ -629,14 +633,16 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
     const uint64_t sc2 = f2(p.scale, p.scale);
     float m_ref = kNegInf, l = 0.f;
     int n = 0;
-    bool ok = true;
+    // FDMA_FLAG_TEST_SHORT_WAIT: a wait on a barrier nothing arrives at expires first
+    bool ok = !p.test_short_wait ||
+              mbar_wait(&bars[k2Never], 0, p.err, kDevErrTimeout, abort_flag, kTestWaitNs);
     uint32_t raw[32];
     // The keep bits of a partial tile are fetched one active tile ahead, so their
     // load latency overlaps the wait for S.
     auto is_partial = [&](int kt) { return map_row[kt] == kPartial || (ragged_k && kt == p.nTk - 1); };
     uint4 bits_next = make_uint4(~0u, ~0u, ~0u, ~0u);
     if (first_kt < p.nTk && is_partial(first_kt)) bits_next = __ldg(&p.bits_row[(tile_base + first_kt) * kTile + r]);
-    for (int kt = first_kt; kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
+    for (int kt = first_kt; ok && kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
       const bool partial = is_partial(kt);
       const uint4 bits = bits_next;
       {

@@ -51,6 +51,7 @@ struct FwdParams {
   int d;  // head dim of q, k, v, out (the kernel runs on its padded width, 64 or 128)
   int bias_bsel, bias_hsel;  // 0 where the bias is broadcast over batch / kv head (TMA coordinate 0)
   float scale, scale_log2;  // softmax scale and scale * log2(e)
+  int test_short_wait;      // FDMA_FLAG_TEST_SHORT_WAIT: the softmax warps time out on purpose
   const int8_t* kmap;
   const uint4* bits_row;
   uint16_t* out;  // (B,Nq,Hq,d)
@@ -86,6 +87,7 @@ struct BwdParams {
   int d;  // head dim of q, k, v, dout, dk, dv (the kernel runs on its padded width)
   int bias_bsel, bias_hsel;  // 0 where the bias is broadcast over batch / kv head (TMA coordinate 0)
   float scale, scale_log2;
+  int test_short_wait;  // FDMA_FLAG_TEST_SHORT_WAIT: the compute warps time out on purpose
   const int8_t* kmap;
   const uint4* bits_col;
   const uint16_t* bias;  // may be null

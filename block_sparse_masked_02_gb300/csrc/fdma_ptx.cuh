@@ -14,6 +14,7 @@ namespace fdma {
 
 // ---------------------------------------------------------------- constants
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legal wait
+constexpr uint64_t kTestWaitNs = 100000ull;       // 100 us: the test wait of FDMA_FLAG_TEST_SHORT_WAIT
 
 // ---------------------------------------------------------------- addresses
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -78,18 +79,18 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
-// Bounded wait for phase `parity` of `bar`.  On time-out writes `code` into
-// *err (first writer wins) and returns false.  A wait also gives up at once
-// when another warp of the CTA has already recorded a failure in *abort_flag
-// (shared memory), so one time-out unwinds the whole CTA quickly.
+// Bounded wait for phase `parity` of `bar`.  On time-out (limit_ns of wall time) writes
+// `code` into *err (first writer wins) and returns false.  A wait also gives up at once
+// when another warp of the CTA has already recorded a failure in *abort_flag (shared
+// memory), so one time-out unwinds the whole CTA quickly.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
     if (abort_flag != nullptr && *abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       atomicCAS(err, 0, code);
       if (abort_flag != nullptr) *abort_flag = 1;
       return false;

@@ -31,6 +31,7 @@ FDMA_MASK_BITS = 5
 
 FDMA_FLAG_REUSE_CLASSIFICATION = 1
 FDMA_FLAG_NO_SKIP = 2
+FDMA_FLAG_TEST_SHORT_WAIT = 4
 
 TILE = 128
 

@@ -77,6 +77,12 @@ typedef enum {
 /* flags */
 #define FDMA_FLAG_REUSE_CLASSIFICATION 1u /* workspace already classified for this mask: skip the classifier */
 #define FDMA_FLAG_NO_SKIP 2u              /* debug: treat every causally allowed tile as PARTIAL (no skipping) */
+#define FDMA_FLAG_TEST_SHORT_WAIT 4u      /* test: in fdma_fwd / fdma_bwd the softmax (compute) warps first wait
+                                             about 100 us on a barrier nothing arrives at; the wait expires,
+                                             the kernel unwinds (its own copies and products drained, TMEM
+                                             freed) and fdma_get_device_error() returns FDMA_ERR_TIMEOUT.
+                                             The outputs are then incomplete.  Exercises the bounded-wait
+                                             failure path without any fault. */
 
 typedef struct fdma_args {
   /* problem size: batch, query length, key length, query heads, kv heads, head dim (64, or a
@@ -143,7 +149,12 @@ FDMA_API size_t fdma_workspace_size(const fdma_args* args, int for_bwd);
 FDMA_API int fdma_classify_blocks(const fdma_args* args, int block_m, int block_n, int8_t* block_map, void* stream);
 
 /* Forward.  Classifies (unless FDMA_FLAG_REUSE_CLASSIFICATION) and computes
-   out: bf16 (B,Nq,Hq,d) contiguous and lse: fp32 (B,Hq,Nq) contiguous. */
+   out: bf16 (B,Nq,Hq,d) contiguous and lse: fp32 (B,Hq,Nq) contiguous.
+   Precision: the softmax weights enter the P V product rounded to bf16, and both O and lse
+   are normalised by the sum of those rounded weights (so the weights that produced O sum to
+   exactly 1).  lse is therefore the log-sum-exp of the definition up to a relative error of
+   the row sum of at most 2^-9: |lse - exact| <= ln(1 + 2^-9) ~ 1.95e-3, plus fp32 rounding.
+   fdma_bwd expects this lse (it recomputes the same weights). */
 FDMA_API int fdma_fwd(const fdma_args* args, void* out, float* lse, void* stream);
 
 /* Backward.  out, dout: bf16 (B,Nq,Hq,d) contiguous; lse as written by fdma_fwd.
@@ -151,7 +162,11 @@ FDMA_API int fdma_fwd(const fdma_args* args, void* out, float* lse, void* stream
    group's query heads), dbias: bf16 (B,Hkv,Nq,Nk) (NULL: not computed; requires
    args->bias != NULL), all contiguous.  Every dbias element is written (zeros in
    skipped tiles and at masked positions).  Classifies unless
-   FDMA_FLAG_REUSE_CLASSIFICATION.  Needs the for_bwd workspace size. */
+   FDMA_FLAG_REUSE_CLASSIFICATION.  Needs the for_bwd workspace size.
+   Determinism: dk, dv and dbias are bitwise reproducible run to run (each is summed in a
+   fixed order inside one CTA).  dq is not: every key tile adds its part to an fp32
+   accumulator with atomic reductions whose order varies, so repeated calls can differ in
+   the last bits of dq (well inside the bf16 rounding of the result). */
 FDMA_API int fdma_bwd(const fdma_args* args, const void* out, const void* dout, const float* lse, void* dq, void* dk,
              void* dv, void* dbias, void* stream);
 

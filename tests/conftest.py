@@ -9,3 +9,9 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (runs the sm_103a kernels)")
     config.addinivalue_line("markers", "slow: long-running case")
+
+
+def pytest_sessionfinish(session, exitstatus):
+    import parity_report
+
+    parity_report.write()

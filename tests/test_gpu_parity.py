@@ -15,6 +15,7 @@ import torch
 
 from oracle import attention as orc
 from block_sparse_masked_02_gb300 import workloads as W
+from parity_report import record
 
 pytestmark = pytest.mark.gpu
 
@@ -42,7 +43,7 @@ def _cuda(t):
     return None if t is None else t.cuda()
 
 
-def run_and_compare(F, inp, causal, scale, want_dbias=True, flags=0, check_bwd=True):
+def run_and_compare(F, inp, causal, scale, want_dbias=True, flags=0, check_bwd=True, case=None):
     q, k, v, do = (_cuda(inp[n]) for n in ("q", "k", "v", "dout"))
     bias, mask, cr = _cuda(inp.get("bias")), _cuda(inp.get("mask")), _cuda(inp.get("colranges"))
     out, lse = F.fwd(q, k, v, mask=mask, colranges=cr, bias=bias, causal=causal, scale=scale, flags=flags)
@@ -61,16 +62,23 @@ def run_and_compare(F, inp, causal, scale, want_dbias=True, flags=0, check_bwd=T
     assert np.abs(o_gpu - O).max() <= O_MAXABS, np.abs(o_gpu - O).max()
     assert rel_l2(o_gpu, O) <= O_RELL2, rel_l2(o_gpu, O)
     fin = ~empty
-    assert np.abs(l_gpu[fin] - L[fin]).max(initial=0.0) <= LSE_ABS
+    lse_err = np.abs(l_gpu[fin] - L[fin]).max(initial=0.0)
+    assert lse_err <= LSE_ABS
+    if case is not None:
+        record(case, o_maxabs=np.abs(o_gpu - O).max(), o_rel_l2=rel_l2(o_gpu, O), lse_maxabs=lse_err)
     if not check_bwd:
         return
     rq, rk, rv, rb = orc.backward(p, want_dbias=(db is not None))
     for name, x, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
         e = rel_l2(x.float().cpu().numpy(), ref)
+        if case is not None:
+            record(case, **{name + "_rel_l2": e})
         assert e <= G_RELL2, (name, e)
     if db is not None:
         dbn = db.float().cpu().numpy()
         e = rel_l2(dbn, rb)
+        if case is not None:
+            record(case, dbias_rel_l2=e)
         assert e <= G_RELL2, ("dbias", e)
         keep = np.zeros(rb.shape, dtype=bool)
         for b in range(p.B):
@@ -81,7 +89,7 @@ def run_and_compare(F, inp, causal, scale, want_dbias=True, flags=0, check_bwd=T
 
 def test_quickstart_workload(F):
     wl = W.WORKLOADS["tiny_n256_d64"]
-    run_and_compare(F, W.make_inputs(wl), True, wl.scale)
+    run_and_compare(F, W.make_inputs(wl), True, wl.scale, case="tiny_n256_d64 (element-wise)")
 
 
 def test_quickstart_workload_loss_sum(F):
@@ -385,3 +393,35 @@ def test_one_head_per_kv_head_with_bias(F):
     wl = W.scaled(W.WORKLOADS["n4096_hq32_hkv8"], Nq=392, Nk=392, Hq=2, Hkv=2, keep_window=128, seed=53)
     inp = W.make_inputs(wl)
     run_and_compare(F, inp, True, wl.scale)
+
+
+@pytest.mark.parametrize("variant", ["bias_g2", "colranges_g3"])
+def test_bounded_wait_unwind(F, variant):
+    """FDMA_FLAG_TEST_SHORT_WAIT makes the softmax / compute warps' first wait expire (a
+    barrier nothing arrives at, ~100 us limit): forward and backward report
+    FDMA_ERR_TIMEOUT through the device error word, unwind without a fault (copies and
+    products drained, TMEM freed), and the next normal calls on the same context match the
+    oracle."""
+    T = F.FDMA_FLAG_TEST_SHORT_WAIT
+    if variant == "bias_g2":  # two-head forward, backward with bias and dBias
+        wl = W.scaled(W.WORKLOADS["n4096_hq32_hkv8"], Nq=512, Nk=512, Hq=4, Hkv=2, keep_window=200, seed=91)
+        inp = W.make_inputs(wl)
+        causal, scale = True, wl.scale
+    else:  # single-head forward (odd group), backward without bias
+        wl = W.Workload("doc_unwind", 1, 384, 384, 3, 1, 64, True, 0.125, "colranges", 0, False, doc_lo=50,
+                        doc_hi=200, seed=92)
+        inp = W.make_inputs(wl)
+        causal, scale = True, wl.scale
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "dout"))
+    kw = dict(mask=_cuda(inp.get("mask")), colranges=_cuda(inp.get("colranges")), bias=_cuda(inp.get("bias")),
+              causal=causal, scale=scale)
+    assert F.device_error() == 0
+    F.fwd(q, k, v, flags=T, **kw)
+    assert F.device_error() == F.FDMA_ERR_TIMEOUT
+    assert F.device_error() == 0  # read and cleared
+    out, lse = F.fwd(q, k, v, **kw)
+    assert F.device_error() == 0
+    F.bwd(q, k, v, out, do, lse, flags=T, **kw)
+    assert F.device_error() == F.FDMA_ERR_TIMEOUT
+    assert F.device_error() == 0
+    run_and_compare(F, inp, causal, scale)
