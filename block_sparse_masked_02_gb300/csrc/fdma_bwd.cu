@@ -31,9 +31,11 @@
 //                    once per (query tile, key tile) through a staged TMA store; the bias
 //                    tile of a query tile is TMA-loaded into shared memory once and each
 //                    thread copies its key column into registers for all heads.  dO is
-//                    double-buffered (with a bias, the second slot is the bias buffer).
-//                    Skipped tiles of dBias are written as zeros by the same CTA.
-//                    Warps: 0 TMA, 1 MMA, 4..11 two compute groups, 12..15 dQ drain.
+//                    double-buffered (with a bias, the second slot is the bias buffer, which a
+//                    second producer thread refills with the next tile's bias).  Skipped
+//                    tiles of dBias are written as zeros by the same CTA.
+//                    Warps: 0 TMA (Q, dO), 1 MMA, 2 TMA (bias), 4..11 two compute groups,
+//                    12..15 dQ drain.
 //   dq_convert       fp32 accumulator -> bf16 dQ.
 #include "fdma_internal.h"
 #include "fdma_ptx.cuh"
@@ -173,7 +175,7 @@ enum BwdBar : int {
   kDoFull = 5,   // +slot (up to 2)
   kDoEmpty = 7,  // +slot (up to 2)
   kBFull = 9,    // bias tile of the current query tile
-  kBEmpty = 10,
+  kBEmpty = 10,  // the tile's bias has been copied out of the bias buffer (compute threads)
   kSFull = 11,
   kDpFull = 12,
   kPReady = 13,   // P^T of the step stored in TMEM (compute threads)
@@ -184,7 +186,8 @@ enum BwdBar : int {
   kFinal = 18,
   kDrain = 19,
   kNever = 20,    // never arrived at: the target of the test wait (FDMA_FLAG_TEST_SHORT_WAIT)
-  kNumBwdBars = 21
+  kBufDone = 21,  // the last dO of a query tile in the bias buffer has been read (one phase per tile)
+  kNumBwdBars = 22
 };
 
 // 16 warps: warpgroup 0 = {TMA producer, MMA issuer, 2 idle}, warpgroups 1-2 = compute,
@@ -242,12 +245,18 @@ struct ColIter {
 
 // dO slot of step n (head hh of its query tile).  Without a bias there are two dO slots,
 // used alternately.  With a bias the second slot is the bias buffer (it directly follows the
-// dO slot): head hh uses it when G-1-hh is odd, so the last head of every query tile uses
-// slot 0 and the buffer is free to receive the next tile's bias during that head.
+// dO slot), which holds a query tile's bias until the compute warps have copied it (right
+// before the tile's first step): the first and the last head of every tile use slot 0, the
+// heads between alternate, so the buffer's last dO use in a tile comes early and the next
+// tile's bias has time to arrive.  With G = 4: slots 0, 1, 0, 0.
 template <bool HAS_BIAS>
 __device__ __forceinline__ int do_slot(int n, int hh, int G) {
-  return HAS_BIAS ? ((G - 1 - hh) & 1) : (n & 1);
+  return HAS_BIAS ? ((hh == G - 1) ? 0 : (hh & 1)) : (n & 1);
 }
+// Number of slot-1 (bias buffer) dO fills in one query tile under do_slot with a bias, and the
+// head of the last of them (-1 when there is none).
+__device__ __forceinline__ int slot1_fills_per_tile(int G) { return (G - 1) / 2; }
+__device__ __forceinline__ int last_slot1_head(int G) { return G >= 3 ? (((G - 2) & 1) ? G - 2 : G - 3) : -1; }
 
 template <int D, bool HAS_BIAS, bool WANT_DBIAS>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -296,10 +305,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBwdBars; ++i) mbar_init(&bars[i], 1);
+    mbar_init(&bars[kBEmpty], 256);
     mbar_init(&bars[kPReady], 256);
     mbar_init(&bars[kDsReady], 256);
     mbar_init(&bars[kDqFree], 128);
-    mbar_init(&bars[kBEmpty], 256);
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -330,26 +339,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmDO);
-    if (HAS_BIAS) tma_prefetch_desc(&tmB);
-    const uint64_t bias_pol = l2_evict_first();  // each bias tile is read once here
     mbar_arrive_expect_tx(&bars[kKVFull], 2 * L::kQB);
 #pragma unroll
     for (int c = 0; c < KB; ++c) {
       tma_load_4d(sK + c * 16384, &tmK, &bars[kKVFull], c * 64, k0, g, b);
       tma_load_4d(sV + c * 16384, &tmV, &bars[kKVFull], c * 64, k0, g, b);
     }
-    int n = 0, qi_count = 0, nbias = 0, nq_issued = 0;
+    int n = 0, qi_count = 0, nq_issued = 0;
     int ufill0 = 0, ufill1 = 0;  // dO fills of slot 0 / slot 1
     bool ok = true;
-    auto load_bias = [&](int qt) {
-      mbar_arrive_expect_tx(&bars[kBFull], 32768);
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
-        tma_load_4d_hint(sBias + c * 16384, &tmB, &bars[kBFull], k0 + c * 64, qt * kTile, g * p.bias_hsel,
-                         b * p.bias_bsel, bias_pol);
-      ++nbias;
-    };
-    if (HAS_BIAS) load_bias(first_qt);  // the first bias tile has no predecessor in its buffer
     for (int qt = first_qt; ok && it.valid(qt); qt = it.next(qt), ++qi_count) {
       for (int hh = 0; hh < p.G; ++hh, ++n) {
         const int h = g * p.G + hh;
@@ -365,8 +363,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         nq_issued = n + 1;
         const int sd = do_slot<HAS_BIAS>(n, hh, p.G);
         const int u = sd ? ufill1 : ufill0;
-        if (HAS_BIAS && sd == 1 && hh == (((p.G - 1) & 1) ? 0 : 1)) {
-          // first use of the bias buffer in this tile: the tile's bias must have been copied out
+        if (HAS_BIAS && sd == 1 && hh == 1) {
+          // first dO in the bias buffer this tile: the tile's bias must have been copied out
           if (!(ok = mbar_wait(&bars[kBEmpty], qi_count & 1, p.err, kDevErrTimeout, abort_flag))) break;
         } else {
           if (!(ok = mbar_wait(&bars[kDoEmpty + sd], (u & 1) ^ 1, p.err, kDevErrTimeout, abort_flag))) break;
@@ -379,17 +377,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         else ufill0 = u + 1;
       }
       if (!ok) break;
-      if (HAS_BIAS) {
-        const int nq = it.next(qt);
-        if (it.valid(nq)) {
-          // the next tile's bias goes into the buffer once its last dO there (or, with one head
-          // per group, this tile's bias) has been released
-          if (p.G >= 2) ok = mbar_wait(&bars[kDoEmpty + 1], (ufill1 - 1) & 1, p.err, kDevErrTimeout, abort_flag);
-          else ok = mbar_wait(&bars[kBEmpty], qi_count & 1, p.err, kDevErrTimeout, abort_flag);
-          if (!ok) break;
-          load_bias(nq);
-        }
-      }
     }
     if (*abort_flag) {
       // let this CTA's own copies land before it retires (bounded waits)
@@ -399,8 +386,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // only the last fill of each slot can still be in flight
       if (ufill0 > 0) mbar_wait(&bars[kDoFull + 0], (ufill0 - 1) & 1, p.err, kDevErrTimeout, nullptr);
       if (ufill1 > 0) mbar_wait(&bars[kDoFull + 1], (ufill1 - 1) & 1, p.err, kDevErrTimeout, nullptr);
-      if (HAS_BIAS && nbias > 0) mbar_wait(&bars[kBFull], (nbias - 1) & 1, p.err, kDevErrTimeout, nullptr);
     }
+   } else if (HAS_BIAS && warp == 2 && lane == 0 && any_active) {
+    // ------------------------------------------------------------ bias producer
+    // One bias tile per active query tile into the bias buffer: the first at once, each
+    // later one as soon as the buffer is free, i.e. once the last dO that went into the
+    // buffer during the previous tile has been read by its products (or, with no such dO,
+    // once the previous tile's bias has been copied out).
+    tma_prefetch_desc(&tmB);
+    const uint64_t bias_pol = l2_evict_first();  // each bias tile is read once here
+    const int per_tile = slot1_fills_per_tile(p.G);
+    int nbias = 0;
+    bool ok = true;
+    for (int qt = first_qt; ok && it.valid(qt); qt = it.next(qt)) {
+      if (nbias > 0) {
+        // kBufDone completes once per tile (an mbarrier parity wait must not fall two phases
+        // behind, so the per-fill kDoEmpty phases are not waited on here)
+        if (per_tile > 0)
+          ok = mbar_wait(&bars[kBufDone], (nbias - 1) & 1, p.err, kDevErrTimeout, abort_flag);
+        else
+          ok = mbar_wait(&bars[kBEmpty], (nbias - 1) & 1, p.err, kDevErrTimeout, abort_flag);
+        if (!ok) break;
+      }
+      mbar_arrive_expect_tx(&bars[kBFull], 32768);
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        tma_load_4d_hint(sBias + c * 16384, &tmB, &bars[kBFull], k0 + c * 64, qt * kTile, g * p.bias_hsel,
+                         b * p.bias_bsel, bias_pol);
+      ++nbias;
+    }
+    // only the last bias fill can still be in flight
+    if (*abort_flag && nbias > 0) mbar_wait(&bars[kBFull], (nbias - 1) & 1, p.err, kDevErrTimeout, nullptr);
    } else if (warp == 1 && lane == 0 && any_active) {
     // ------------------------------------------------------------ MMA issuer
     bool ok = mbar_wait(&bars[kKVFull], 0, p.err, kDevErrTimeout, abort_flag);
@@ -462,6 +478,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                                                   (n > 0 || k > 0) ? 1u : 0u);
         });
         umma_commit(&bars[kDoEmpty + sd]);  // dP^T(n) and dV(n) have read this dO slot
+        if (HAS_BIAS && hh == last_slot1_head(p.G)) umma_commit(&bars[kBufDone]);  // the buffer's last dO this tile
         if (sd) ++uuse1;
         else ++uuse0;
         if (!(ok = mbar_wait(&bars[kDsReady], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
@@ -526,20 +543,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // No compute thread leaves these loops early, so every one of them reaches every named
     // barrier below; after a failed wait (ok == false) the work and the stores are skipped.
     // Per query tile: the keep bits of queries qbase..qbase+63 for key j and the bias^T column
-    // slice, copied once into registers for every head.  The next tile's are fetched right
-    // after the P pass of the current tile's last head, the only pass that uses them.
+    // slice, copied once into registers for every head (only the P passes use them).
     uint32_t bw0 = ~0u, bw1 = ~0u;
     uint32_t bpk[HAS_BIAS ? 32 : 1];
-    auto fetch_tile = [&](int qt, int qi) {
-      const bool partial = it.cls(qt) == kPartial || ragged_k || (ragged_q_any && qt == p.nTq - 1);
-      bw0 = ~0u;
-      bw1 = ~0u;
-      if (partial) {
+    // keep bits of queries qbase..qbase+63 for key j in query tile qt (all ones unless partial)
+    auto load_bits = [&](int qt) -> uint2 {
+      uint2 bb = make_uint2(~0u, ~0u);
+      if (it.valid(qt) && (it.cls(qt) == kPartial || ragged_k || (ragged_q_any && qt == p.nTq - 1))) {
         const int64_t tile = col_base + static_cast<int64_t>(qt) * p.nTk;
-        const uint2 bb = reinterpret_cast<const uint2*>(&p.bits_col[tile * kTile + j])[wg];
-        bw0 = bb.x;
-        bw1 = bb.y;
+        bb = reinterpret_cast<const uint2*>(&p.bits_col[tile * kTile + j])[wg];
       }
+      return bb;
+    };
+    // the tile's keep bits (loaded one tile ahead) and bias^T slice, into registers
+    auto fetch_tile = [&](const uint2 bits, int qi) {
+      bw0 = bits.x;
+      bw1 = bits.y;
       if (HAS_BIAS) {
         ok = ok && mbar_wait(&bars[kBFull], qi & 1, p.err, kDevErrTimeout, abort_flag);
         const uint8_t* bt = sBias + (j >> 6) * 16384 + (j & 7) * 2;
@@ -557,39 +576,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(&bars[kBEmpty]);
       }
     };
-    // Once the steps that read the dS^T tile are done (kDsFree), stage the summed dBias of the
-    // query tile at q0t in it as a (query, key) SW128 tile and TMA-store it; the caller waits
-    // for the store's read before the tile is written again.
-    auto stage_dbias = [&](int q0t) {
-      uint8_t* dbt = sDS + (j >> 6) * 16384 + (j & 7) * 2;
-      const int jc = (j & 63) >> 3;
+    // Write the summed dBias of the query tile at q0t straight from registers, pairs of
+    // queries qp0 .. qp0+NP-1: thread (key j) holds its key's column slice (64 queries); one
+    // lane shuffle per pair of queries trades halves with the neighbouring key so that each
+    // thread stores two adjacent keys of one row (4 bytes), and a warp instruction writes two
+    // contiguous 64-byte row segments.
+    auto store_dbias = [&](int q0t, int qp0, auto npc) {
+      constexpr int NP = decltype(npc)::value;
       const uint64_t inv2 = f2(1.f / p.scale, 1.f / p.scale);  // the sums are of scale * dS
+      const bool odd = (j & 1) != 0;
+      const int col = kidx & ~1;  // this thread's pair of keys: col, col + 1
+      uint32_t* base = reinterpret_cast<uint32_t*>(
+          p.dbias + ((static_cast<int64_t>(b) * p.Hkv + g) * p.Nq + q0t + qbase + (odd ? 1 : 0)) * p.Nk + col);
+      const int64_t row2 = p.Nk;  // two rows of bf16, in 4-byte words
 #pragma unroll
-      for (int qp = 0; qp < 32; ++qp) {
-        const int i = qbase + 2 * qp;
+      for (int qp = qp0; qp < qp0 + NP; ++qp) {
         float a0, a1;
         f2split(mul2(acc2[qp], inv2), a0, a1);
-        const uint32_t w = pack_bf16x2(a0, a1);
-        if (ok) {
-          *reinterpret_cast<uint16_t*>(dbt + i * 128 + ((jc ^ (i & 7)) << 4)) = static_cast<uint16_t>(w & 0xFFFFu);
-          *reinterpret_cast<uint16_t*>(dbt + (i + 1) * 128 + ((jc ^ ((i + 1) & 7)) << 4)) =
-              static_cast<uint16_t>(w >> 16);
-        }
+        const uint32_t w = pack_bf16x2(a0, a1);  // (query 2qp, query 2qp+1) of key j
+        // even key: keeps its row-2qp value, sends its row-2qp+1 value; odd key the reverse
+        const uint32_t send = odd ? (w & 0xFFFFu) : (w >> 16);
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, send, 1);
+        // row 2qp (even thread): (key col, key col+1) = (w.lo, got); row 2qp+1 (odd thread):
+        // (key col, key col+1) = (got, w.hi)
+        const uint32_t pair = odd ? (got | (w & 0xFFFF0000u)) : ((w & 0xFFFFu) | (got << 16));
+        const int row = q0t + qbase + 2 * qp + (odd ? 1 : 0);
+        if (ok && row < p.Nq && kin) base[qp * row2] = pair;
         acc2[qp] = 0ull;
       }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 256);
-      if (ctid == 0 && ok) {
-        const uint64_t pol = l2_evict_first();  // dBias is written once, never read here
-        tma_store_4d_hint(&tmDB, sDS, k0, q0t, g, b, pol);
-        tma_store_4d_hint(&tmDB, sDS + 16384, k0 + 64, q0t, g, b, pol);
-        bulk_commit_group();
-      }
     };
-    if (any_active) fetch_tile(first_qt, 0);
     int q0_prev = 0;
+    uint2 bits_next = load_bits(first_qt);
     for (int qt = first_qt; it.valid(qt); qt = it.next(qt), ++qi_count) {
       const int q0 = qt * kTile;
+      // the previous tile's dBias (complete after its last dS pass), then this tile's keep
+      // bits and bias^T slice, right before its first P pass; the next tile's keep bits are
+      // requested now so that their load is hidden behind this tile's steps
+      if (WANT_DBIAS && qi_count > 0) store_dbias(q0_prev, 0, std::integral_constant<int, 32>{});
+      fetch_tile(bits_next, qi_count);
+      bits_next = load_bits(it.next(qt));
       for (int hh = 0; hh < p.G; ++hh, ++n) {
         const int s = n & 1;
         // ---------------- P pass: P^T = exp2(S^T * scale*log2e + bias^T*log2e - lse*log2e)
@@ -634,20 +659,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_before();
           mbar_arrive(&bars[kPReady]);
         }
-        if (hh == p.G - 1) {  // the bits and bias^T slice of this tile are no longer needed
-          const int nq = it.next(qt);
-          if (it.valid(nq)) fetch_tile(nq, qi_count + 1);
-        }
         // ---------------- dS pass: scale * dS^T = P^T (scale * dP^T - scale * delta)
         ok = ok && mbar_wait(&bars[kDpFull], n & 1, p.err, kDevErrTimeout, abort_flag);
-        if (WANT_DBIAS && hh == 0 && qi_count > 0) {
-          // the previous query tile's dBias goes out through the dS^T tile first, once the
-          // previous step's dQ and dK products have read that tile
-          ok = ok && mbar_wait(&bars[kDsFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag);
-          stage_dbias(q0_prev);
-          if (ctid == 0) bulk_wait_read_all();
-          named_bar_sync(1, 256);
-        }
         if (ok) {
           tc_fence_after();
           const float* dlt = sDelta + s * 128 + qbase;
@@ -700,16 +713,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       q0_prev = q0;
     }
-    if (WANT_DBIAS && n > 0) {
-      // the last query tile's dBias, once its last step's products are done with dS^T
-      ok = ok && mbar_wait(&bars[kDsFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag);
-      stage_dbias(q0_prev);
-    }
+    if (WANT_DBIAS && n > 0)  // the last query tile's dBias
+      store_dbias(q0_prev, 0, std::integral_constant<int, 32>{});
     if (ok && n > 0) ok = mbar_wait(&bars[kFinal], 0, p.err, kDevErrTimeout, abort_flag);
     // zero-fill the dBias tiles of this key column that were skipped (TMA stores of a zero tile)
     if (WANT_DBIAS) {
-      if (ctid == 0) bulk_wait_read_all();  // the last tile's dBias store has read the dS^T tile
-      named_bar_sync(1, 256);
+      // every product has finished with the dS^T tile (kFinal): it becomes the zero tile
       reinterpret_cast<uint4*>(sDS)[ctid * 8 + 0] = make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int u = 1; u < 8; ++u) reinterpret_cast<uint4*>(sDS)[ctid * 8 + u] = make_uint4(0, 0, 0, 0);

@@ -97,8 +97,11 @@ def test_quickstart_workload_loss_sum(F):
     run_and_compare(F, W.make_inputs(wl, dout_ones=True), True, wl.scale)
 
 
-@pytest.mark.parametrize("N,Hq,Hkv,d,keep", [(512, 8, 2, 128, 256), (328, 4, 2, 128, 100), (384, 4, 4, 64, 64)])
+@pytest.mark.parametrize("N,Hq,Hkv,d,keep", [(512, 8, 2, 128, 256), (328, 4, 2, 128, 100), (384, 4, 4, 64, 64),
+                                             (640, 8, 1, 128, 200), (520, 6, 1, 64, 150), (392, 10, 2, 128, 120)])
 def test_causal_topk(F, N, Hq, Hkv, d, keep):
+    """Causal top-k masks with a bias, GQA group sizes 1, 2, 4, 5, 6 and 8 (the backward
+    keeps one to three dO tiles per query tile in the bias buffer) and ragged tails."""
     wl = W.scaled(W.WORKLOADS["n4096_hq32_hkv8"], Nq=N, Nk=N, Hq=Hq, Hkv=Hkv, d=d, keep_window=keep,
                   scale=1 / math.sqrt(d), seed=77 + N)
     run_and_compare(F, W.make_inputs(wl), True, wl.scale)
