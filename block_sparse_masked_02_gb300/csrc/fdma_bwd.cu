@@ -573,6 +573,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const bool k0b = (wd >> ((2 * e) & 31)) & 1u, k1b = (wd >> ((2 * e + 1) & 31)) & 1u;
           bpk[e] = (k0b ? lo : 0xFF80u) | ((k1b ? hi : 0xFF80u) << 16);
         }
+        // The buffer is next written by TMA (the async proxy): the proxy fence orders these
+        // generic reads before that write.  Without it the write was seen to overtake reads
+        // still in flight (head dim 64, dO into the buffer right after the release).
+        fence_proxy_async_smem();
         mbar_arrive(&bars[kBEmpty]);
       }
     };
@@ -635,7 +639,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               nl[2 * v] = a.x;
               nl[2 * v + 1] = a.y;
             }
-            tmem_ld_wait();
+            tmem_ld_wait(sr);
             const uint32_t word = c < 2 ? bw0 : bw1;
             uint32_t pk[8];
 #pragma unroll
@@ -677,7 +681,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               dd[2 * v] = bq.x;
               dd[2 * v + 1] = bq.y;
             }
-            tmem_ld_wait();
+            tmem_ld_wait(dr);
+            tmem_ld_tie(pp);
             uint32_t dk[8];
 #pragma unroll
             for (int e = 0; e < 16; e += 2) {
@@ -747,7 +752,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t r[32];
         if (n > 0) {
           tmem_ld32(tl + col0 + c * 32, r);
-          tmem_ld_wait();
+          tmem_ld_wait(r);
         } else {
 #pragma unroll
           for (int t = 0; t < 32; ++t) r[t] = 0u;
@@ -788,7 +793,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld32(tl + 160, r1);
           tmem_ld32(tl + 192, r2);
           tmem_ld32(tl + 224, r3);
-          tmem_ld_wait();
+          tmem_ld_wait(r0);
+          tmem_ld_tie(r1);
+          tmem_ld_tie(r2);
+          tmem_ld_tie(r3);
           tc_fence_before();
           mbar_arrive(&bars[kDqFree]);
           // The accumulator is interleaved by four queries (dq_acc_index), so each thread adds
@@ -820,7 +828,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint32_t r0[32], r1[32];
           tmem_ld32(tl + 128, r0);
           tmem_ld32(tl + 160, r1);
-          tmem_ld_wait();
+          tmem_ld_wait(r0);
+          tmem_ld_tie(r1);
           tc_fence_before();
           mbar_arrive(&bars[kDqFree]);
           float* dqrow = p.dq_acc + dq_acc_index(b, h, q0 + row, 0, p.Hq, p.nqpad, D);

@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         tmem_ld32(tl + s * 128 + c * 32, raw);
-        tmem_ld_wait();
+        tmem_ld_wait(raw);
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[c * 32 + j] = __uint_as_float(raw[j]) * p.scale_log2;
       }
@@ -280,6 +280,7 @@ __global__ void __launch_bounds__(192, 1)
             x[cc * 8 + 2 * e + 1] = fmaf(__uint_as_float(w[e] & 0xFFFF0000u), kLog2e, x[cc * 8 + 2 * e + 1]);
           }
         }
+        fence_proxy_async_smem();  // generic reads of the slot before its next TMA write
         mbar_arrive(&bars[kBEmpty + s]);
       }
       if (partial) {
@@ -315,7 +316,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           tmem_ld32(tl + 256 + c * 32, raw);
-          tmem_ld_wait();
+          tmem_ld_wait(raw);
           uint32_t lo[16], hi[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -357,7 +358,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int c = 0; c < D / 32; ++c) {
         if (n > 0) {
           tmem_ld32(tl + 256 + c * 32, raw);
-          tmem_ld_wait();
+          tmem_ld_wait(raw);
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) raw[j] = 0u;
@@ -665,6 +666,7 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) u[cc * 4 + e] = bf16x2_to_f2(wv[e]);
         }
+        fence_proxy_async_smem();  // generic reads of the slot before its next TMA write
         mbar_arrive(&bars[k2BEmpty + sb]);
       } else if (partial) {
 #pragma unroll
@@ -686,7 +688,7 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         tmem_ld32(tl + scol + c * 32, raw);
-        tmem_ld_wait();
+        tmem_ld_wait(raw);
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
           const uint64_t s2 = f2(__uint_as_float(raw[2 * t]), __uint_as_float(raw[2 * t + 1]));
@@ -732,7 +734,7 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
         for (int c = 0; c < D / 16; ++c) {
           uint32_t o16[16];
           tmem_ld16(tl + ocol + c * 16, o16);
-          tmem_ld_wait();
+          tmem_ld_wait(o16);
 #pragma unroll
           for (int j = 0; j < 16; ++j) o16[j] = __float_as_uint(__uint_as_float(o16[j]) * alpha);
           tmem_st16(tl + ocol + c * 16, o16);
@@ -776,7 +778,7 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
       for (int c = 0; c < D / 32; ++c) {
         if (n > 0) {
           tmem_ld32(tl + ocol + c * 32, raw);
-          tmem_ld_wait();
+          tmem_ld_wait(raw);
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) raw[j] = 0u;
