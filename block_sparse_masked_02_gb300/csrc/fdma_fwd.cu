@@ -339,7 +339,8 @@ __global__ void __launch_bounds__(192, 1)
           const float p1 = ex2(x[c * 32 + 2 * j + 1] - mu);
           pk[j] = pack_bf16x2(p0, p1);
           // normalise with the same bf16-rounded weights the PV product uses
-          sum4[j & 3] += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xFFFF0000u);
+          sum4[2 * (j & 1)] = add_bf16lo(pk[j], sum4[2 * (j & 1)]);
+          sum4[2 * (j & 1) + 1] = add_bf16hi(pk[j], sum4[2 * (j & 1) + 1]);
         }
         tmem_st16(tl + s * 128 + c * 16, pk);
       }
@@ -742,7 +743,7 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
       }
       const float nm = (m_ref == kNegInf) ? 0.f : -(m_ref * cexp);
       const uint64_t nm2 = f2(nm, nm);
-      uint64_t sum2[2] = {0ull, 0ull};
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};  // (even pairs, odd pairs) x (low, high) halves
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
@@ -752,7 +753,9 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
           f2split(fma2(u[c * 16 + j], c2, nm2), e0, e1);
           const float p0 = ex2(e0), p1 = ex2(e1);
           pk[j] = pack_bf16x2(p0, p1);
-          sum2[j & 1] = add2(sum2[j & 1], bf16x2_to_f2(pk[j]));  // the row sum of P as rounded for PV
+          // the row sum of P as rounded for PV
+          sum4[2 * (j & 1)] = add_bf16lo(pk[j], sum4[2 * (j & 1)]);
+          sum4[2 * (j & 1) + 1] = add_bf16hi(pk[j], sum4[2 * (j & 1) + 1]);
         }
         tmem_st16(tl + scol + c * 16, pk);
         if (c & 1) {  // keys 0..63 (c = 1), then 64..127 (c = 3): that half of PV may start
@@ -762,10 +765,7 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
         }
       }
       {
-        const uint64_t s2 = add2(sum2[0], sum2[1]);
-        float s0, s1;
-        f2split(s2, s0, s1);
-        l += s0 + s1;
+        l += (sum4[0] + sum4[2]) + (sum4[1] + sum4[3]);
       }
     }
     // ------------------------------------------------------------------ epilogue

@@ -457,6 +457,23 @@ __device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) {
   return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
+// c + the low / high bf16 of a pair, in one mixed-precision add of sm_100+ (the bf16 value is
+// widened exactly, then one round-to-nearest add: the same result as widening first).
+__device__ __forceinline__ float add_bf16lo(uint32_t w, float c) {
+  float r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, lo, %2;\n\t}"
+      : "=f"(r)
+      : "r"(w), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float add_bf16hi(uint32_t w, float c) {
+  float r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, hi, %2;\n\t}"
+      : "=f"(r)
+      : "r"(w), "f"(c));
+  return r;
+}
+
 // ---------------------------------------------------------------- packing
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
