@@ -510,7 +510,7 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
 #pragma unroll
         for (int c = 0; c < KB; ++c)
           tma_load_4d(sQ + w * L::kQB + c * 16384, &tmQ, &bars[k2QFull], c * 64, q0, h0 + w, b);
-      int n = 0, items = 0;
+      int n = 0, items = 0, nbias = 0;
       bool ok = true;
       for (int kt = first_kt; ok && kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
         const int k0 = kt * kTile;
@@ -532,6 +532,7 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
           for (int c = 0; c < 2; ++c)
             tma_load_4d_hint(sB + sb * L::kBB + c * 16384, &tmB, &bars[k2BFull + sb], k0 + c * 64, q0, g * p.bias_hsel,
                              b * p.bias_bsel, bias_pol);
+          nbias = n + 1;
         }
         // V_n
         {
@@ -548,6 +549,9 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
         mbar_wait(&bars[k2QFull], 0, p.err, kDevErrTimeout, nullptr);
         for (int it = items > 3 ? items - 3 : 0; it < items; ++it)
           mbar_wait(&bars[k2KvFull + it % 3], (it / 3) & 1, p.err, kDevErrTimeout, nullptr);
+        // and the last fill of each bias slot
+        for (int m = nbias > 2 ? nbias - 2 : 0; m < nbias; ++m)
+          mbar_wait(&bars[k2BFull + (m & 1)], (m >> 1) & 1, p.err, kDevErrTimeout, nullptr);
       }
     } else if (warp == 1 && lane == 0 && any_active) {
       // ---------------------------------------------------------------- MMA issuer

@@ -21,7 +21,10 @@ constexpr int kTopkMaxKeys = 65536;  // one row's keys held in shared memory
 // below 64 would need 64-byte-swizzled tiles: the 64-column box cannot be wider than the
 // tensor.)
 inline int padded_head_dim(int d) { return d <= 64 ? 64 : 128; }
-inline bool head_dim_ok(int d) { return d == 64 || (d > 64 && d <= 128 && d % 8 == 0); }
+// Head dims: multiples of 8 from 8 to 128.  The kernels are built for 64 and 128; a smaller
+// head dim runs on the next one up, the missing columns of Q, K, V and dO read as zeros by TMA
+// (out-of-range fill) and the padding columns of the results never stored.
+inline bool head_dim_ok(int d) { return d >= 8 && d <= 128 && d % 8 == 0; }
 constexpr int kSkip = 0, kPartial = 1, kFull = 2;
 
 // Device error word values (first writer wins).

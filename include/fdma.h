@@ -85,8 +85,9 @@ typedef enum {
                                              failure path without any fault. */
 
 typedef struct fdma_args {
-  /* problem size: batch, query length, key length, query heads, kv heads, head dim (64, or a
-     multiple of 8 from 72 to 128; other values: FDMA_ERR_UNSUPPORTED) */
+  /* problem size: batch, query length, key length, query heads, kv heads, head dim (a multiple
+     of 8 from 8 to 128, run on the 64- or 128-wide kernels with the missing columns read as
+     zeros; other values: FDMA_ERR_UNSUPPORTED) */
   int32_t B, Nq, Nk, Hq, Hkv, d;
 
   /* q (B,Nq,Hq,d), k and v (B,Nk,Hkv,d); strides in ELEMENTS for (batch, seq, head); the

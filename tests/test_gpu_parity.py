@@ -390,6 +390,22 @@ def test_other_head_dims(F, d, Hq, Hkv):
     run_and_compare(F, inp, True, wl.scale)
 
 
+@pytest.mark.parametrize("d,Hq,Hkv,kind", [(32, 4, 2, "bias"), (32, 3, 1, "colranges"), (16, 4, 2, "bias"),
+                                           (48, 2, 2, "bias"), (8, 4, 1, "colranges"), (56, 6, 2, "bias")])
+def test_small_head_dims(F, d, Hq, Hkv, kind):
+    """Head dims below 64 (multiples of 8) run on the 64-wide kernels with the missing columns
+    of Q, K, V and dO read as zeros: outputs and all four gradients match the oracle, for the
+    two-head and the one-head forward (even and odd group sizes)."""
+    if kind == "bias":
+        wl = W.scaled(W.WORKLOADS["n4096_hq32_hkv8"], Nq=392, Nk=392, Hq=Hq, Hkv=Hkv, d=d, keep_window=110,
+                      seed=70 + d + Hq, scale=1.0 / math.sqrt(d))
+    else:
+        wl = W.Workload("doc_small_d", 1, 392, 392, Hq, Hkv, d, True, 1.0 / math.sqrt(d), "colranges", 0, False,
+                        doc_lo=60, doc_hi=180, seed=80 + d + Hq)
+    inp = W.make_inputs(wl)
+    run_and_compare(F, inp, True, wl.scale, case=f"d{d}_hq{Hq}_hkv{Hkv}_{kind}")
+
+
 def test_one_head_per_kv_head_with_bias(F):
     """G = 1 with a bias: the backward keeps one dO slot and reloads the bias buffer after each
     query tile's bias copy (no second dO slot to alternate with)."""

@@ -77,7 +77,7 @@ def test_workspace_size_arithmetic(F):
 
 
 @pytest.mark.parametrize("field,value,status", [
-    ("scale", float("nan"), 1), ("scale", -1.0, 1), ("Hq", 3, 1), ("d", 100, 2), ("d", 136, 2), ("d", 32, 2),
+    ("scale", float("nan"), 1), ("scale", -1.0, 1), ("Hq", 3, 1), ("d", 100, 2), ("d", 136, 2), ("d", 36, 2), ("d", 0, 2),
     ("Nk", 0, 1),
     ("mask_kind", 7, 1), ("mask_kind", 1, 1), ("mask_kind", 3, 1), ("mask_kind", 4, 1), ("Hkv", 0, 1),
 ])
