@@ -55,6 +55,8 @@ int validate(const fdma_args* a, bool need_workspace) {
   if (!head_dim_ok(a->d)) return FDMA_ERR_UNSUPPORTED;
   if (cdiv(a->Nk, kTile) > kMaxKTiles || cdiv(a->Nq, kTile) > kMaxKTiles) return FDMA_ERR_UNSUPPORTED;
   if (!(std::isfinite(a->scale) && a->scale > 0.f)) return FDMA_ERR_INVALID;
+  if (a->is_causal < 0 || a->is_causal > 2) return FDMA_ERR_INVALID;
+  if (a->is_causal == 2 && (a->q_offset > (1 << 30) || a->q_offset < -(1 << 30))) return FDMA_ERR_INVALID;
   if (a->q == nullptr || a->k == nullptr || a->v == nullptr) return FDMA_ERR_INVALID;
   for (const void* p : {a->q, a->k, a->v})
     if (!aligned16(p)) return FDMA_ERR_UNSUPPORTED;
@@ -148,7 +150,7 @@ int classify_into_workspace(const fdma_args* a, int8_t* user_map, cudaStream_t s
   p.nTk = cdiv(a->Nk, kTile);
   p.mask_kind = a->mask_kind;
   p.causal = a->is_causal ? 1 : 0;
-  p.causal_off = a->Nk - a->Nq;
+  p.causal_off = a->is_causal == 2 ? a->q_offset : a->Nk - a->Nq;
   p.no_skip = (a->flags & FDMA_FLAG_NO_SKIP) ? 1 : 0;
   p.mask = static_cast<const uint16_t*>(a->mask);
   p.mask_u8 = static_cast<const uint8_t*>(a->mask);

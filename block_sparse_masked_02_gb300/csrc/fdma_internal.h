@@ -37,7 +37,7 @@ constexpr int kDevErrAlign = FDMA_ERR_CUDA;
 struct ClassifyParams {
   int B, Nq, Nk, Hkv, nTq, nTk;
   int mask_kind, causal, no_skip;
-  int causal_off;  // Nk - Nq: key j is visible from query i when j <= i + causal_off
+  int causal_off;  // key j is visible from query i when j <= i + causal_off (Nk - Nq, or q_offset)
   const uint16_t* mask;
   const uint8_t* mask_u8;  // same buffer, FDMA_MASK_DENSE_U8 / FDMA_MASK_BITS
   int64_t ms_b, ms_h, ms_r;

@@ -52,6 +52,7 @@ class FdmaArgs(ctypes.Structure):
         ("bias", ctypes.c_void_p), ("bias_stride", ctypes.c_int64 * 3),
         ("is_causal", ctypes.c_int32), ("scale", ctypes.c_float), ("flags", ctypes.c_uint32),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("q_offset", ctypes.c_int32),
     ]
 
 
@@ -146,11 +147,13 @@ def pack_mask(mask: torch.Tensor) -> PackedMask:
 
 
 def make_args(q, k, v, *, mask=None, colranges=None, bias=None, causal=False, scale=None, workspace=None,
-              flags=0) -> FdmaArgs:
+              flags=0, causal_offset=None) -> FdmaArgs:
     """Fill fdma_args from tensors: q (B,Nq,Hq,d), k/v (B,Nk,Hkv,d) with a contiguous
     head dim; mask (B,Hkv,Nq,Nk) bf16, uint8 or bool and bias (B,Hkv,Nq,Nk) bf16 with
     contiguous columns (stride 0 broadcasts a batch or head axis); colranges int32
-    (B,Hkv,Nk,2) (one masked row range per key) or (B,Hkv,Nk,4) (two)."""
+    (B,Hkv,Nk,2) (one masked row range per key) or (B,Hkv,Nk,4) (two).  causal=True keeps
+    keys j <= i + (Nk - Nq); with causal_offset=c (an int) keys j <= i + c instead, i.e. the
+    query rows are rows c - (Nk - Nq_full) ... of a longer causal problem (is_causal 2)."""
     a = FdmaArgs()
     a.B, a.Nq, a.Hq, a.d = (int(x) for x in q.shape)
     a.Nk, a.Hkv = int(k.shape[1]), int(k.shape[2])
@@ -188,7 +191,11 @@ def make_args(q, k, v, *, mask=None, colranges=None, bias=None, causal=False, sc
             raise ValueError("bias must be bf16 with contiguous columns")
         a.bias = bias.data_ptr()
         a.bias_stride[:] = [bias.stride(0), bias.stride(1), bias.stride(2)]
-    a.is_causal = 1 if causal else 0
+    if causal_offset is not None:
+        a.is_causal = 2
+        a.q_offset = int(causal_offset)
+    else:
+        a.is_causal = 1 if causal else 0
     a.scale = float(scale) if scale is not None else float(a.d) ** -0.5
     a.flags = int(flags)
     if workspace is not None:
@@ -222,10 +229,11 @@ def _raise(status: int, where: str):
         raise FdmaError(status, where)
 
 
-def classify_blocks(q, k, v, *, mask=None, colranges=None, causal=False, workspace=None, flags=0, stream=None):
+def classify_blocks(q, k, v, *, mask=None, colranges=None, causal=False, workspace=None, flags=0, stream=None,
+                    causal_offset=None):
     """Tile classes int8 (B, Hkv, ceil(Nq/128), ceil(Nk/128)): 0 skip, 1 partial, 2 full."""
     _check_cuda(q, k, v, mask, colranges, workspace)
-    args = make_args(q, k, v, mask=mask, colranges=colranges, causal=causal, flags=flags)
+    args = make_args(q, k, v, mask=mask, colranges=colranges, causal=causal, flags=flags, causal_offset=causal_offset)
     ws = workspace if workspace is not None else alloc_workspace(args, False, q.device)
     _attach(args, ws)
     B, Nq, Hkv, Nk = q.shape[0], q.shape[1], k.shape[2], k.shape[1]
@@ -267,10 +275,11 @@ def topk_mask(bias, keep_window, *, mask_dtype=torch.bfloat16, fill_bias=True, i
 
 
 def fwd(q, k, v, *, mask=None, colranges=None, bias=None, causal=False, scale=None, workspace=None, flags=0,
-        out=None, lse=None, stream=None):
+        out=None, lse=None, stream=None, causal_offset=None):
     """Returns (out (B,Nq,Hq,d) bf16, lse (B,Hq,Nq) fp32)."""
     _check_cuda(q, k, v, mask, colranges, bias, workspace)
-    args = make_args(q, k, v, mask=mask, colranges=colranges, bias=bias, causal=causal, scale=scale, flags=flags)
+    args = make_args(q, k, v, mask=mask, colranges=colranges, bias=bias, causal=causal, scale=scale, flags=flags,
+                     causal_offset=causal_offset)
     ws = workspace if workspace is not None else alloc_workspace(args, False, q.device)
     _attach(args, ws)
     B, Nq, Hq, d = q.shape
@@ -283,13 +292,14 @@ def fwd(q, k, v, *, mask=None, colranges=None, bias=None, causal=False, scale=No
 
 
 def bwd(q, k, v, out, dout, lse, *, mask=None, colranges=None, bias=None, causal=False, scale=None,
-        want_dbias=True, workspace=None, flags=0, grads=None, stream=None):
+        want_dbias=True, workspace=None, flags=0, grads=None, stream=None, causal_offset=None):
     """Returns (dq, dk, dv, dbias-or-None)."""
     _check_cuda(q, k, v, out, dout, lse, mask, colranges, bias, workspace)
     for name, t in (("out", out), ("dout", dout), ("lse", lse)):
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
-    args = make_args(q, k, v, mask=mask, colranges=colranges, bias=bias, causal=causal, scale=scale, flags=flags)
+    args = make_args(q, k, v, mask=mask, colranges=colranges, bias=bias, causal=causal, scale=scale, flags=flags,
+                     causal_offset=causal_offset)
     ws = workspace if workspace is not None else alloc_workspace(args, True, q.device)
     _attach(args, ws)
     if grads is None:
@@ -311,12 +321,13 @@ def device_error(stream=None) -> int:
 
 
 def fwd_noalloc(q, k, v, *, mask=None, colranges=None, bias=None, causal=False, scale=None, flags=0, out=None,
-                lse=None, stream=None):
+                lse=None, stream=None, causal_offset=None):
     """Forward through fdma_fwd_noalloc: the library's fixed 16 MiB device array serves as
     the workspace, so nothing is allocated for it (out and lse are allocated here only when
     not given).  Returns (out, lse)."""
     _check_cuda(q, k, v, mask, colranges, bias)
-    args = make_args(q, k, v, mask=mask, colranges=colranges, bias=bias, causal=causal, scale=scale, flags=flags)
+    args = make_args(q, k, v, mask=mask, colranges=colranges, bias=bias, causal=causal, scale=scale, flags=flags,
+                     causal_offset=causal_offset)
     B, Nq, Hq, d = q.shape
     if out is None:
         out = torch.empty((B, Nq, Hq, d), dtype=torch.bfloat16, device=q.device)

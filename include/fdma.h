@@ -128,12 +128,21 @@ typedef struct fdma_args {
   int64_t bias_stride[3];
 
   int32_t is_causal; /* 1: keep additionally requires j <= i + (Nk - Nq) (bottom-right aligned:
-                        j <= i when Nq == Nk; rows that see no key are fully masked) */
+                        j <= i when Nq == Nk); 2: keep requires j <= i + q_offset (below); 0: no
+                        causal rule; other values FDMA_ERR_INVALID.  Rows that see no key are
+                        fully masked. */
   float scale;       /* multiplies Q K^T only; must be finite and > 0 */
   uint32_t flags;    /* FDMA_FLAG_* */
 
   void* workspace; /* device memory, >= fdma_workspace_size(args, for_bwd) bytes, 256-byte aligned */
   size_t workspace_bytes;
+
+  /* is_causal == 2 only: the position of query row 0 in the key sequence, so that query row i
+     sees keys j <= i + q_offset.  A slice of query rows [r0, r1) of a longer causal problem
+     over the same keys is the problem on those rows with q_offset = r0 + (Nk - Nq_full) (context
+     parallelism: each rank's rows against all keys).  |q_offset| <= 2^30, else
+     FDMA_ERR_INVALID.  Ignored for is_causal 0 and 1. */
+  int32_t q_offset;
 } fdma_args;
 
 /* Bytes of workspace needed by fdma_classify_blocks / fdma_fwd (for_bwd = 0) or by

@@ -17,8 +17,14 @@ Definition followed (Flash-DMA README, "Quick Start" example and
                                                             row range per key column,
                                                             or two, masked as a union)
                   | True                                    (no mask)
-                  and (j <= i + Nk - Nq if causal)          (bottom-right aligned; j <= i
-                                                            for square problems)
+                  and (j <= i + c if causal)                (c = Nk - Nq: bottom-right
+                                                            aligned, j <= i for square
+                                                            problems; or a given row offset
+                                                            c: the rows are rows c - (Nk - N) ..
+                                                            of a longer causal problem over the
+                                                            same keys, as one rank of a
+                                                            context-parallel split holds them,
+                                                            FlashMask README, "CPB")
     s_ij = scale * q_i . k_j + bias[b,g,i,j]   if keep, else -inf
     P    = softmax_j(s),  O_i = sum_j P_ij v_j,  lse_i = max_j s_ij + ln sum_j exp(s_ij - max)
 
@@ -72,19 +78,22 @@ class Problem:
     """Inputs of one attention call, as given to both implementations.
 
     q (B,Nq,Hq,d), k/v (B,Nk,Hkv,d), dout like q; bias and mask (B,Hkv,Nq,Nk)
-    or None; colranges (B,Hkv,Nk,2) or (B,Hkv,Nk,4) int or None; mask_bits: the mask
+    or None; colranges (B,Hkv,Nk,2) or (B,Hkv,Nk,4) int or None; causal_offset: the causal
+    rule's row offset (default Nk - Nq); mask_bits: the mask
     bit-packed, uint8 (B,Hkv,Nq,ceil(Nk/8)), key j of a row = bit j % 8 of byte j // 8.
     Tensors may be torch (any dtype, any device) or numpy; slices are converted to float64
     on demand.
     """
 
     def __init__(self, q, k, v, *, bias=None, mask=None, colranges=None, causal=False, scale=None, dout=None,
-                 mask_bits=None):
+                 mask_bits=None, causal_offset=None):
         self.q, self.k, self.v = q, k, v
         self.bias, self.mask, self.colranges, self.mask_bits = bias, mask, colranges, mask_bits
         self.causal = bool(causal)
         self.B, self.Nq, self.Hq, self.d = (int(s) for s in q.shape)
         self.Nk, self.Hkv = int(k.shape[1]), int(k.shape[2])
+        # key j is visible from query row i when j <= i + causal_offset (if causal)
+        self.causal_offset = self.Nk - self.Nq if causal_offset is None else int(causal_offset)
         assert self.Hq % self.Hkv == 0
         self.G = self.Hq // self.Hkv
         self.scale = 1.0 / math.sqrt(self.d) if scale is None else float(scale)
@@ -112,7 +121,7 @@ def keep_rows(p: Problem, b: int, g: int, r0: int, r1: int) -> np.ndarray:
     else:
         keep = np.ones((r1 - r0, p.Nk), dtype=bool)
     if p.causal:
-        keep = keep & (j <= i + (p.Nk - p.Nq))
+        keep = keep & (j <= i + p.causal_offset)
     return keep
 
 

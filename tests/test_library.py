@@ -78,7 +78,7 @@ def test_workspace_size_arithmetic(F):
 
 @pytest.mark.parametrize("field,value,status", [
     ("scale", float("nan"), 1), ("scale", -1.0, 1), ("Hq", 3, 1), ("d", 100, 2), ("d", 136, 2), ("d", 36, 2), ("d", 0, 2),
-    ("Nk", 0, 1),
+    ("Nk", 0, 1), ("is_causal", 3, 1), ("is_causal", -1, 1),
     ("mask_kind", 7, 1), ("mask_kind", 1, 1), ("mask_kind", 3, 1), ("mask_kind", 4, 1), ("Hkv", 0, 1),
 ])
 def test_argument_validation_before_any_cuda_call(F, field, value, status):
@@ -135,3 +135,14 @@ def test_binding_refuses_cpu_tensors_and_bad_packed_masks(F):
         F.PackedMask(torch.zeros(1, 1, 4, 3, dtype=torch.uint8), 16)  # ceil(16/8) = 2 bytes per row
     pm = F.PackedMask(torch.zeros(1, 1, 4, 3, dtype=torch.uint8), 17)
     assert pm.nk == 17 and not pm.is_cuda
+
+
+def test_causal_row_offset_is_range_checked_before_any_cuda_call(F):
+    lib = F.load()
+    for off, want in (((1 << 30) + 1, 1), (-(1 << 30) - 1, 1)):
+        a = _args(F, is_causal=2)
+        a.q_offset = off
+        assert lib.fdma_fwd(ctypes.byref(a), 1 << 20, 1 << 20, None) == want
+    a = _args(F, is_causal=1)
+    a.q_offset = 1 << 31 - 1  # ignored unless is_causal == 2
+    assert lib.fdma_workspace_size(ctypes.byref(a), 1) > 0

@@ -97,6 +97,52 @@ def test_matches_torch_sdpa(Hq, Hkv, causal, with_mask):
         assert np.abs(a - b).max() < 1e-10 * max(1.0, np.abs(b).max())
 
 
+@pytest.mark.parametrize("Nq,Nk,offset", [(37, 70, 0), (37, 70, 20), (37, 70, -4), (40, 40, 17), (70, 37, -50)])
+def test_causal_row_offset_matches_torch_tril(Nq, Nk, offset):
+    """causal_offset=c keeps key j for query row i when j <= i + c: the keep set is torch's
+    lower triangle with diagonal c (torch.tril), and outputs and gradients equal SDPA's on it.
+    With c = Nk - Nq it is the default bottom-right rule; rows [c, c + Nq) of a square causal
+    problem of length Nk see exactly these keys (one rank's rows in a context-parallel split)."""
+    p = _problem(43 + offset, B=1, Nq=Nq, Nk=Nk, Hq=2, Hkv=1, d=8, causal=True, mask="dense", density=0.8, scale=0.5)
+    p.causal_offset = offset
+    O, lse = orc.forward(p)
+    dq, dk, dv, dbias = orc.backward(p)
+    keep = (p.mask != 0) & torch.ones(Nq, Nk, dtype=torch.bool).tril(diagonal=offset)
+    live = keep.any(dim=-1)
+    q = p.q.permute(0, 2, 1, 3).clone().requires_grad_(True)
+    k = p.k.permute(0, 2, 1, 3).clone().requires_grad_(True)
+    v = p.v.permute(0, 2, 1, 3).clone().requires_grad_(True)
+    bias = p.bias.clone().requires_grad_(True)
+    am = bias.masked_fill(~keep, float("-inf")).masked_fill(~live[..., None], 0.0).repeat_interleave(p.G, dim=1)
+    out = torch.nn.functional.scaled_dot_product_attention(
+        q, k.repeat_interleave(p.G, dim=1), v.repeat_interleave(p.G, dim=1), attn_mask=am, scale=p.scale)
+    live_h = live.repeat_interleave(p.G, dim=1)
+    (out * (p.dout.permute(0, 2, 1, 3) * live_h[..., None])).sum().backward()
+    lv = live_h.permute(0, 2, 1).numpy()
+    assert np.abs(O[lv] - out.detach().permute(0, 2, 1, 3).numpy()[lv]).max() < 1e-10
+    assert np.all(O[~lv] == 0.0) and np.all(np.isneginf(lse.transpose(0, 2, 1)[~lv]))
+    for a, b in ((dq, q.grad), (dk, k.grad), (dv, v.grad)):
+        b = b.permute(0, 2, 1, 3).numpy()
+        assert np.abs(a - b).max() < 1e-10 * max(1.0, np.abs(b).max())
+    rdb = bias.grad.masked_fill(~live[..., None], 0.0).numpy()
+    assert np.abs(dbias - rdb).max() < 1e-10 * max(1.0, np.abs(rdb).max())
+    if offset == Nk - Nq:
+        p.causal_offset = None
+        assert np.array_equal(orc.forward(orc.Problem(p.q, p.k, p.v, bias=p.bias, mask=p.mask, causal=True,
+                                                      scale=p.scale))[0], O)
+    if Nq + offset <= Nk and offset >= 0:
+        # the same rows inside the square problem of length Nk (rows offset .. offset + Nq)
+        g = torch.Generator().manual_seed(7)
+        qf = torch.randn(1, Nk, 2, 8, generator=g, dtype=torch.float64)
+        qf[:, offset:offset + Nq] = p.q
+        mf = torch.ones(1, 1, Nk, Nk, dtype=torch.float64)
+        mf[:, :, offset:offset + Nq] = p.mask
+        bf = torch.zeros(1, 1, Nk, Nk, dtype=torch.float64)
+        bf[:, :, offset:offset + Nq] = p.bias
+        Of, _ = orc.forward(orc.Problem(qf, p.k, p.v, bias=bf, mask=mf, causal=True, scale=p.scale))
+        assert np.abs(Of[:, offset:offset + Nq] - O).max() < 1e-12
+
+
 @pytest.mark.parametrize("Nq,Nk", [(37, 70), (70, 37), (64, 64)])
 def test_bottom_right_causal_matches_torch_lower_right_bias(Nq, Nk):
     """Causal alignment when Nq != Nk: torch's own lower-right causal bias
