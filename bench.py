@@ -41,7 +41,7 @@ KERNELS_PER_STEP = 5  # classify, fwd, bwd_pre, bwd, dq_convert
 # the current kernel; a workload without an entry reports null.  n16384_hq16_hkv4: one kv
 # group of the workload (Hq=4, Hkv=1) read 374,551,040 and wrote 539,735,808 bytes; the
 # four kv groups are independent CTAs with the same work, so the full launch moves 4x that.
-BWD_TRAFFIC_BYTES = {"n16384_hq16_hkv4": 4 * (374551040 + 539735808)}
+BWD_TRAFFIC_BYTES = {"n16384_hq16_hkv4": 4 * (373651456 + 539467776)}
 E2E_MAX_HOST_BYTES = 24e9  # larger workloads report no end-to-end number (pinned host copies)
 
 
