@@ -1,0 +1,132 @@
+"""Seeded random problems across the argument space, each against the fp64 oracle: batch, head
+counts and group sizes, query and key lengths (ragged, rectangular), head dims 8..128, every
+mask kind (bf16 / uint8 / bit-packed dense masks, one or two column ranges, none), full and
+broadcast biases, the three causal modes (none, bottom-right, explicit row offset), with and
+without dBias.  Tolerances as in test_gpu_parity.py, except that O's absolute bound carries a
+relative term: O comes back in bf16 (half an ulp is up to 2^-8 of |O|) and is normalised by
+bf16-rounded weights, so a row with few kept keys and |O| near 4 is off by ~0.014 (measured:
+seed 1039, 13 kept keys, O = 4.2047, returned 4.21875, the nearest bf16)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as orc
+
+pytestmark = pytest.mark.gpu
+
+O_MAXABS, O_RELL2, G_RELL2, LSE_ABS = 1e-2, 5e-3, 1e-2, 4e-3
+
+
+@pytest.fixture(scope="module")
+def F():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_sparse_masked_02_gb300 import fdma
+
+    fdma.load()
+    return fdma
+
+
+def rel_l2(x, ref):
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.linalg.norm(ref)
+    return np.linalg.norm(x - ref) / (den if den > 0 else 1.0)
+
+
+def _case(seed):
+    rng = np.random.default_rng(seed)
+    g = torch.Generator().manual_seed(seed)
+    B = int(rng.integers(1, 3))
+    Hkv = int(rng.integers(1, 4))
+    G = int(rng.integers(1, 5))
+    Hq = G * Hkv
+    d = 8 * int(rng.integers(1, 17))
+    mask_kind = rng.choice(["none", "dense", "u8", "bits", "colranges", "colranges2"])
+    bias_kind = rng.choice(["none", "full", "bcast_b", "bcast_h"])
+    if mask_kind in ("dense", "u8") or bias_kind != "none":
+        Nk = 8 * int(rng.integers(1, 90))  # row strides of dense masks and biases: multiples of 8
+    else:
+        Nk = int(rng.integers(1, 700))
+    Nq = int(rng.integers(1, 700))
+    causal = int(rng.integers(0, 3))
+    offset = int(rng.integers(-Nq // 2, Nk + 1)) if causal == 2 else None
+    scale = float(rng.uniform(0.05, 0.3))
+    want_dbias = bool(rng.integers(0, 2))
+
+    def bf(*shape):
+        return torch.randn(*shape, generator=g).to(torch.bfloat16)
+
+    q, k, v, do = bf(B, Nq, Hq, d), bf(B, Nk, Hkv, d), bf(B, Nk, Hkv, d), bf(B, Nq, Hq, d)
+    bias = None
+    if bias_kind == "full":
+        bias = bf(B, Hkv, Nq, Nk)
+    elif bias_kind == "bcast_b":
+        bias = bf(1, Hkv, Nq, Nk).expand(B, Hkv, Nq, Nk)
+    elif bias_kind == "bcast_h":
+        bias = bf(B, 1, Nq, Nk).expand(B, Hkv, Nq, Nk)
+    mask = colranges = None
+    density = float(rng.uniform(0.05, 0.9))
+    if mask_kind in ("dense", "u8", "bits"):
+        keep = torch.rand(B, Hkv, Nq, Nk, generator=g) < density
+        # some all-masked and all-kept 128-blocks, so that every tile class occurs
+        for _ in range(3):
+            qt, kt = int(rng.integers(0, (Nq + 127) // 128)), int(rng.integers(0, (Nk + 127) // 128))
+            keep[..., qt * 128:(qt + 1) * 128, kt * 128:(kt + 1) * 128] = bool(rng.integers(0, 2))
+        mask = keep.to(torch.bfloat16) if mask_kind == "dense" else keep.to(torch.uint8)
+    elif mask_kind.startswith("colranges"):
+        s = torch.randint(-10, Nq + 10, (B, Hkv, Nk), generator=g)
+        ln = torch.randint(-5, max(2, Nq), (B, Hkv, Nk), generator=g)
+        cr = torch.stack([s, s + ln], dim=-1)
+        if mask_kind == "colranges2":
+            s2 = torch.randint(-10, Nq + 10, (B, Hkv, Nk), generator=g)
+            cr = torch.cat([cr, torch.stack([s2, s2 + torch.randint(0, 64, (B, Hkv, Nk), generator=g)], dim=-1)], -1)
+        colranges = cr.to(torch.int32).contiguous()
+    return dict(B=B, Nq=Nq, Nk=Nk, Hq=Hq, Hkv=Hkv, d=d, q=q, k=k, v=v, do=do, bias=bias, mask=mask,
+                mask_kind=mask_kind, colranges=colranges, causal=causal, offset=offset, scale=scale,
+                want_dbias=want_dbias)
+
+
+@pytest.mark.parametrize("seed", list(range(1000, 1040)))
+def test_random_problem_matches_oracle(F, seed):
+    c = _case(seed)
+    cuda = lambda t: None if t is None else t.cuda()
+    q, k, v, do = (cuda(c[n]) for n in ("q", "k", "v", "do"))
+    bias = cuda(c["bias"])
+    mask = cuda(c["mask"])
+    if c["mask_kind"] == "bits":
+        mask = F.pack_mask(mask)
+    kw = dict(mask=mask, colranges=cuda(c["colranges"]), bias=bias, scale=c["scale"],
+              causal=c["causal"] == 1, causal_offset=c["offset"] if c["causal"] == 2 else None)
+    out, lse = F.fwd(q, k, v, **kw)
+    dq, dk, dv, db = F.bwd(q, k, v, out, do, lse, want_dbias=c["want_dbias"], **kw)
+    assert F.device_error() == 0
+    p = orc.Problem(c["q"], c["k"], c["v"], bias=c["bias"], mask=c["mask"], colranges=c["colranges"],
+                    causal=c["causal"] != 0, causal_offset=c["offset"], scale=c["scale"], dout=c["do"])
+    O, L = orc.forward(p)
+    o = out.float().cpu().numpy()
+    l = lse.cpu().numpy()
+    empty = np.isneginf(L)
+    assert np.array_equal(np.isneginf(l), empty)
+    assert np.all(o.transpose(0, 2, 1, 3)[empty] == 0.0)
+    err = np.abs(o - O)
+    if err.size:
+        b_, i_, h_, c_ = np.unravel_index(np.argmax(err), err.shape)
+        nkeep = int(orc.keep_rows(p, b_, h_ // (c["Hq"] // c["Hkv"]), i_, i_ + 1).sum())
+        where = f"row {i_} head {h_} col {c_}: kept keys {nkeep}, |O| {abs(O[b_, i_, h_, c_]):.3f}"
+    # O is returned in bf16 and normalised by bf16-rounded weights: up to 2^-9 relative each,
+    # which a row of few keys with |O| near 2-4 turns into more than 1e-2 absolute
+    assert np.all(err <= O_MAXABS + 2.0 ** -7 * np.abs(O)), where
+    assert rel_l2(o, O) <= O_RELL2
+    fin = ~empty
+    assert np.abs(l[fin] - L[fin]).max(initial=0.0) <= LSE_ABS
+    want_db = c["want_dbias"] and c["bias"] is not None
+    assert (db is not None) == want_db
+    rq, rk, rv, rb = orc.backward(p, want_dbias=want_db)
+    for name, x, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)) + ((("db", db, rb),) if want_db else ()):
+        x = x.float().cpu().numpy()
+        assert x.shape == ref.shape, name
+        if np.abs(ref).max(initial=0.0) == 0.0:
+            assert np.all(x == 0.0), name  # nothing reaches this gradient
+        else:
+            assert rel_l2(x, ref) <= G_RELL2, (name, rel_l2(x, ref))
