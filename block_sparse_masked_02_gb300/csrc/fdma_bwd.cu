@@ -15,15 +15,15 @@
 //                                              pairs, or the keep bits without a bias)
 //                      scale*dS^T = P^T (scale*dP^T - scale*delta)
 //                      dV  += P^T dO          (TS: P^T packed in TMEM cols 0..31, 64..95)
-//                      dK  += dS^T Q          (TS: dS^T packed in TMEM cols 128..159, 192..223)
-//                      dQ^T = K^T dS^T        (SS: dS^T also staged in smem; TMEM cols 128..;
+//                      dQ^T = K^T dS^T        (SS: dS^T staged in smem; TMEM cols 128..;
 //                                              for d = 64 computed as dQ = dS K)
+//                      dK  += dS^T Q          (SS, the same dS^T tile)
 //                    Four roles: a TMA producer, a single-thread MMA issuer, two compute
 //                    warpgroups and a dQ drain warpgroup.  The compute warps run each step
 //                    in two passes, P (right after S^T) and dS (after dP^T); the MMA order
-//                    per step is dV(n) once P^T(n) is stored, then S^T(n+1), dK(n), dQ(n),
+//                    per step is dV(n) once P^T(n) is stored, then S^T(n+1), dQ(n), dK(n),
 //                    dP^T(n+1) once dS^T(n) is stored, so the next step's P pass overlaps
-//                    the products.  The drain warps read dQ out of TMEM and add it to an fp32
+//                    the products and the drain reads dQ(n) out of TMEM while dK(n) runs.  The drain warps read dQ out of TMEM and add it to an fp32
 //                    accumulator with paced 16-byte reductions.  The softmax scale is folded
 //                    into dS (delta comes scaled from the preprocess), so dQ and dK need no
 //                    further scaling.  dBias = sum over the group's heads of dS is kept in
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr bool DQ_T = (D == 128);  // dQ^T = K^T dS^T (lane = head-dim index) for coalesced reductions
   constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);   // S^T, dP^T
   constexpr uint32_t IDESC_DV = idesc_bf16(128, D, false, true);     // P^T(tmem) x dO (N contiguous)
-  constexpr uint32_t IDESC_DK = idesc_bf16(128, D, false, true);     // dS^T(tmem) x Q (N contiguous)
+  constexpr uint32_t IDESC_DK = idesc_bf16(128, D, false, true);     // dS^T (K contiguous) x Q (N contiguous)
   constexpr uint32_t IDESC_DQ = DQ_T ? idesc_bf16(128, 128, true, true)   // K^T (M=d contiguous) x dS^T
                                      : idesc_bf16(128, D, true, true);    // dS (M contiguous) x K
 
@@ -425,6 +425,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t vdesc_k = sdesc_sw128(smem_u32(sV), 16, 1024);
     const uint64_t kdesc_mn = sdesc_sw128(smem_u32(sK), 16384, 1024);
     const uint64_t dsdesc_mn = sdesc_sw128(smem_u32(sDS), 16384, 1024);
+    const uint64_t dsdesc_k = sdesc_sw128(smem_u32(sDS), 16, 1024);
     const uint64_t q0desc_k = sdesc_sw128(smem_u32(sQ), 16, 1024);
     const uint64_t q0desc_mn = sdesc_sw128(smem_u32(sQ), 16384, 1024);
     const uint64_t do0desc_k = sdesc_sw128(smem_u32(sDO), 16, 1024);
@@ -459,11 +460,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       return true;
     };
     // Per step n: dV(n) as soon as P^T(n) is stored (it overlaps the dS pass), then, once
-    // dS^T(n) is stored, S^T(n+1), dK(n), dQ(n), dP^T(n+1).  The compute warps start on
-    // P^T(n+1) as soon as S^T(n+1) is done.  dK(n) reads dS^T(n) from TMEM (packed by the dS
-    // pass into the dP^T columns it has read) before dQ(n) overwrites those columns, and it
-    // frees the Q slot early for the load two steps ahead; the drain warps read dQ(n) out of
-    // TMEM before dP^T(n+1) needs its columns.
+    // dS^T(n) is stored, S^T(n+1), dQ(n), dK(n), dP^T(n+1).  The compute warps start on
+    // P^T(n+1) as soon as S^T(n+1) is done; the drain warps read dQ(n) out of TMEM (over the
+    // dP^T columns) while dK(n) runs, so dP^T(n+1) can follow dK(n) at once.  dQ(n) and dK(n)
+    // both take dS^T from shared memory; dK(n) frees the Q slot for the load two steps ahead.
     ok = ok && issue_s(0) && issue_dp(0, do_slot<HAS_BIAS>(0, 0, p.G));
     for (int qt = first_qt; ok && it.valid(qt); qt = it.next(qt)) {
       for (int hh = 0; hh < p.G; ++hh, ++n) {
@@ -485,14 +485,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         const bool more = hh + 1 < p.G || it.valid(it.next(qt));
         if (more && !(ok = issue_s(n + 1))) break;  // over P^T(n), which dV(n) and the dS pass have read
-        // dK += dS^T Q  (TS: dS^T packed in TMEM cols 128..159 and 192..223)
-        static_for<0, 8>([&](auto kc) {
-          constexpr int k = decltype(kc)::value;
-          umma_ts_off<128 + k * 8 + (k >= 4 ? 32 : 0), mnmajor_off(k)>(tbase + 384, tbase, qdesc_mn, IDESC_DK,
-                                                                        (n > 0 || k > 0) ? 1u : 0u);
-        });
-        umma_commit(&bars[kQEmpty + s]);
-        // dQ (K dimension = 128 keys) over the dP^T columns, after dK has read dS^T there
+        // dQ (K dimension = 128 keys) over the dP^T columns, first: the drain reads it out of
+        // TMEM while dK runs
         static_for<0, 8>([&](auto kc) {
           constexpr int k = decltype(kc)::value;
           if (DQ_T)
@@ -501,6 +495,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             umma_ss_off<mnmajor_off(k), mnmajor_off(k)>(tbase + 128, dsdesc_mn, kdesc_mn, IDESC_DQ, k > 0);
         });
         umma_commit(&bars[kDqFull]);
+        // dK += dS^T Q  (SS: dS^T K-major in shared memory)
+        static_for<0, 8>([&](auto kc) {
+          constexpr int k = decltype(kc)::value;
+          umma_ss_off<kmajor_off(k), mnmajor_off(k)>(tbase + 384, dsdesc_k, qdesc_mn, IDESC_DK, (n > 0 || k > 0) ? 1u : 0u);
+        });
+        umma_commit(&bars[kQEmpty + s]);
         umma_commit(&bars[kDsFree]);  // the shared-memory dS^T tile has been read
         if (more) {
           const int hn = hh + 1 < p.G ? hh + 1 : 0;
@@ -695,10 +695,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               f2split(dv2, d0, d1);
               dk[e >> 1] = pack_bf16x2(d0, d1);
             }
-            // packed dS^T for the dK product, in this warpgroup's dP^T columns already read:
-            // queries 0..63 -> cols 128..159, queries 64..127 -> cols 192..223
-            tmem_st8(tl + 128 + wg * 64 + c * 8, dk);
-            // the previous step's dQ must have read the shared-memory dS^T tile
+            // the previous step's dQ and dK must have read the shared-memory dS^T tile
             if (c == 0 && n > 0 && !mbar_wait(&bars[kDsFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag)) {
               ok = false;
               break;
@@ -710,7 +707,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           if (ok) {
             fence_proxy_async_smem();
-            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bars[kDsReady]);
           }
