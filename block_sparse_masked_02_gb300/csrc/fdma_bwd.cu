@@ -132,38 +132,41 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const DqConvertParams p
       make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(c.x, c.y), pack_bf16x2(c.z, c.w));
 }
 
-// 128-wide accumulator interleaved by four query rows (dq_acc_index): one thread per
-// (batch, head, group of four queries, eight head-dim indices) reads 128 contiguous bytes
-// and writes eight bf16 of each of the four query rows.
+// dQ accumulator (interleaved by four queries) -> bf16 dQ for the 128-wide kernels.  A CTA
+// converts 32 query rows of one (batch, head): it reads their 16 KB of the accumulator with
+// coalesced 16-byte loads into shared memory (4 floats of padding after every 8 head-dim
+// indices, so that the transposed reads below hit 32 different banks), then each thread
+// packs 8 head-dim indices of one query row and stores them as 16 bytes.
+constexpr int kCvtGroups = 8;                 // groups of four query rows per CTA
+constexpr int kCvtGroupFloats = 128 * 4 + 64;  // one group in shared memory, padded
 __global__ void __launch_bounds__(256) dq_convert4_kernel(const DqConvertParams p) {
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+  __shared__ __align__(16) float tile[kCvtGroups * kCvtGroupFloats];
   const int nqg = p.nqpad >> 2;
-  const int64_t total = static_cast<int64_t>(p.B) * p.Hq * nqg * 16;
-  if (t >= total) return;
-  const int c8 = static_cast<int>(t & 15) * 8;  // first head-dim index
-  const int64_t rest = t >> 4;
-  const int qg = static_cast<int>(rest % nqg);
-  const int64_t bh = rest / nqg;
-  const int h = static_cast<int>(bh % p.Hq);
-  const int b = static_cast<int>(bh / p.Hq);
-  if (c8 >= p.d) return;  // head-dim padding
-  const float4* src = reinterpret_cast<const float4*>(p.dq_acc + (bh * nqg + qg) * 512 + c8 * 4);
-  float v[8][4];
+  const int blocks_per_bh = nqg / kCvtGroups;
+  const int bh = blockIdx.x / blocks_per_bh;
+  const int g0 = (blockIdx.x % blocks_per_bh) * kCvtGroups;
+  const int h = bh % p.Hq, b = bh / p.Hq;
+  const float4* src = reinterpret_cast<const float4*>(p.dq_acc + (static_cast<int64_t>(bh) * nqg + g0) * 512);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const float4 x = src[e];
-    v[e][0] = x.x;
-    v[e][1] = x.y;
-    v[e][2] = x.z;
-    v[e][3] = x.w;
+  for (int k = 0; k < 4; ++k) {
+    const int idx = threadIdx.x + 256 * k;  // group * 128 + head-dim index: its four queries
+    const int grp = idx >> 7, c = idx & 127;
+    const float4 v = __ldcs(src + idx);     // read once
+    *reinterpret_cast<float4*>(&tile[grp * kCvtGroupFloats + c * 4 + (c >> 3) * 4]) = v;
   }
+  __syncthreads();
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r4 = lane & 3;
+  const int i = (g0 + w) * 4 + r4;  // query row
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int i = qg * 4 + r;
-    if (i >= p.Nq) break;
-    *reinterpret_cast<uint4*>(p.dq + ((static_cast<int64_t>(b) * p.Nq + i) * p.Hq + h) * p.d + c8) =
-        make_uint4(pack_bf16x2(v[0][r], v[1][r]), pack_bf16x2(v[2][r], v[3][r]), pack_bf16x2(v[4][r], v[5][r]),
-                   pack_bf16x2(v[6][r], v[7][r]));
+  for (int half = 0; half < 2; ++half) {
+    const int c8 = (lane >> 2) + 8 * half;  // head-dim indices 8*c8 .. 8*c8+7
+    if (c8 * 8 >= p.d || i >= p.Nq) continue;
+    // index 8*c8 + e of query r4 sits at 36*c8 + 4*e + r4 of the group
+    const float* t = &tile[w * kCvtGroupFloats + 36 * c8 + r4];
+    *reinterpret_cast<uint4*>(p.dq + ((static_cast<int64_t>(b) * p.Nq + i) * p.Hq + h) * p.d + c8 * 8) =
+        make_uint4(pack_bf16x2(t[0], t[4]), pack_bf16x2(t[8], t[12]), pack_bf16x2(t[16], t[20]),
+                   pack_bf16x2(t[24], t[28]));
   }
 }
 
@@ -881,9 +884,9 @@ cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream) {
 
 cudaError_t launch_dq_convert(const DqConvertParams& p, cudaStream_t stream) {
   if (p.dpad == 128) {
-    const int64_t total = static_cast<int64_t>(p.B) * p.Hq * (p.nqpad / 4) * 16;
-    if (total == 0) return cudaSuccess;
-    dq_convert4_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(p);
+    const int64_t blocks = static_cast<int64_t>(p.B) * p.Hq * (p.nqpad / 4) / kCvtGroups;  // nqpad % 128 == 0
+    if (blocks == 0) return cudaSuccess;
+    dq_convert4_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
     return cudaGetLastError();
   }
   const int64_t total = static_cast<int64_t>(p.B) * p.Nq * p.Hq * p.d / 8;
