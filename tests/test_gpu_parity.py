@@ -292,6 +292,44 @@ def test_block_map_bit_exact(F, case):
     assert np.array_equal(bm.cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("layout", ["bcast_b", "bcast_h", "padded_rows", "one_row"])
+@pytest.mark.parametrize("causal", [False, True, -300, 1000, 5000])
+def test_dense_mask_layouts_classify_exactly(F, layout, causal):
+    """bf16 and uint8 masks give the same tile classes (equal to the oracle's) and bit-identical
+    outputs through a mask broadcast over the batch or kv-head axis (stride 0), a padded row
+    stride, a single query row, and the causal modes (bottom-right, explicit row offsets on both
+    sides of the keys), with and without tile skipping."""
+    g = torch.Generator().manual_seed(57)
+    B, Hkv, Hq, Nq, Nk = 2, 2, 4, 392, 264
+    if layout == "one_row":
+        Nq = 1
+    q = torch.randn(B, Nq, Hq, 64, generator=g).bfloat16()
+    k = torch.randn(B, Nk, Hkv, 64, generator=g).bfloat16()
+    v = torch.randn(B, Nk, Hkv, 64, generator=g).bfloat16()
+    shape = {"bcast_b": (1, Hkv), "bcast_h": (B, 1)}.get(layout, (B, Hkv))
+    keep = torch.rand(*shape, Nq, Nk, generator=g) < 0.05
+    keep[..., : min(Nq, 128), 128:256] = True  # a full tile (unless the causal rule cuts it)
+    keep[..., 128:256, 0:128] = False  # an empty one
+    mask = keep.bfloat16()
+    if layout == "padded_rows":
+        mask = torch.zeros(B, Hkv, Nq, Nk + 40).bfloat16()
+        mask[..., :Nk] = keep.bfloat16()
+        mask = mask[..., :Nk]
+    mask = mask.expand(B, Hkv, Nq, Nk)
+    kw = dict(causal=causal is True, causal_offset=None if isinstance(causal, bool) else causal)
+    qc, kc, vc, mc = q.cuda(), k.cuda(), v.cuda(), mask.cuda()
+    m8 = mask.to(torch.uint8).contiguous().cuda()
+    bm = F.classify_blocks(qc, kc, vc, mask=mc, **kw)
+    assert torch.equal(bm, F.classify_blocks(qc, kc, vc, mask=m8, **kw))
+    p = orc.Problem(q, k, k, mask=mask.contiguous(), causal=causal is not False, causal_offset=kw["causal_offset"])
+    assert np.array_equal(bm.cpu().numpy(), orc.classify_blocks(p))
+    for flags in (0, F.FDMA_FLAG_NO_SKIP):
+        a = F.fwd(qc, kc, vc, mask=mc, scale=0.125, flags=flags, **kw)
+        b = F.fwd(qc, kc, vc, mask=m8, scale=0.125, flags=flags, **kw)
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    assert F.device_error() == 0
+
+
 def test_reuse_classification(F):
     wl = W.scaled(W.WORKLOADS["tiny_n256_d64"], seed=6)
     inp = W.make_inputs(wl)
