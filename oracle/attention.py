@@ -28,7 +28,9 @@ Definition followed (Flash-DMA README, "Quick Start" example and
     s_ij = scale * q_i . k_j + bias[b,g,i,j]   if keep, else -inf
     P    = softmax_j(s),  O_i = sum_j P_ij v_j,  lse_i = max_j s_ij + ln sum_j exp(s_ij - max)
 
-Query head h reads kv head g = h // (Hq / Hkv).  A row with no kept key has
+Query head h reads kv head g = h // (Hq / Hkv).  v (and so O, dO, dV) may have a
+head dim dv other than the d of q and k (FlashMask README, "Performance": the SM100
+head-dim table lists d = 192 with dv = 128).  A row with no kept key has
 O_i = 0, lse_i = -inf and contributes nothing to any gradient.  The scale
 multiplies Q K^T only; the bias is added unscaled.
 
@@ -92,6 +94,7 @@ class Problem:
         self.causal = bool(causal)
         self.B, self.Nq, self.Hq, self.d = (int(s) for s in q.shape)
         self.Nk, self.Hkv = int(k.shape[1]), int(k.shape[2])
+        self.dv = int(v.shape[3])  # head dim of v, O and dO (d for q and k)
         # key j is visible from query row i when j <= i + causal_offset (if causal)
         self.causal_offset = self.Nk - self.Nq if causal_offset is None else int(causal_offset)
         assert self.Hq % self.Hkv == 0
@@ -130,7 +133,7 @@ def _kv(p: Problem, b: int, g: int):
 
 
 def forward_rows(p: Problem, b: int, h: int, r0: int, r1: int, kv=None, keep=None):
-    """O (R,d), lse (R,), P (R,Nk) for query head h, rows [r0, r1)."""
+    """O (R,dv), lse (R,), P (R,Nk) for query head h, rows [r0, r1)."""
     g = h // p.G
     K, V = _kv(p, b, g) if kv is None else kv
     if keep is None:
@@ -154,8 +157,8 @@ def forward_rows(p: Problem, b: int, h: int, r0: int, r1: int, kv=None, keep=Non
 
 
 def forward(p: Problem, row_block: int = 1024):
-    """Full O (B,Nq,Hq,d) and lse (B,Hq,Nq), float64."""
-    O = np.zeros((p.B, p.Nq, p.Hq, p.d))
+    """Full O (B,Nq,Hq,dv) and lse (B,Hq,Nq), float64."""
+    O = np.zeros((p.B, p.Nq, p.Hq, p.dv))
     lse = np.zeros((p.B, p.Hq, p.Nq))
     for b in range(p.B):
         for g in range(p.Hkv):
@@ -172,7 +175,7 @@ def backward_rows(p: Problem, b: int, g: int, r0: int, r1: int, kv=None, keep=No
     """Gradient pieces produced by query rows [r0, r1) of kv group g.
 
     Returns dq (R,G,d) for those rows, the rows' additive contributions
-    dk_part / dv_part (Nk,d), and dbias rows (R,Nk) (sum over the group's heads).
+    dk_part (Nk,d) / dv_part (Nk,dv), and dbias rows (R,Nk) (sum over the group's heads).
     """
     K, V = _kv(p, b, g) if kv is None else kv
     if keep is None:
@@ -180,7 +183,7 @@ def backward_rows(p: Problem, b: int, g: int, r0: int, r1: int, kv=None, keep=No
     R = r1 - r0
     dq = np.zeros((R, p.G, p.d))
     dk = np.zeros((p.Nk, p.d))
-    dv = np.zeros((p.Nk, p.d))
+    dv = np.zeros((p.Nk, p.dv))
     dbias = np.zeros((R, p.Nk))
     for hh in range(p.G):
         h = g * p.G + hh
@@ -198,11 +201,11 @@ def backward_rows(p: Problem, b: int, g: int, r0: int, r1: int, kv=None, keep=No
 
 
 def backward(p: Problem, row_block: int = 1024, want_dbias: bool = True):
-    """Full dq (B,Nq,Hq,d), dk/dv (B,Nk,Hkv,d), dbias (B,Hkv,Nq,Nk) or None."""
+    """Full dq (B,Nq,Hq,d), dk (B,Nk,Hkv,d), dv (B,Nk,Hkv,dv), dbias (B,Hkv,Nq,Nk) or None."""
     assert p.dout is not None
     dq = np.zeros((p.B, p.Nq, p.Hq, p.d))
     dk = np.zeros((p.B, p.Nk, p.Hkv, p.d))
-    dv = np.zeros((p.B, p.Nk, p.Hkv, p.d))
+    dv = np.zeros((p.B, p.Nk, p.Hkv, p.dv))
     dbias = np.zeros((p.B, p.Hkv, p.Nq, p.Nk)) if want_dbias else None
     for b in range(p.B):
         for g in range(p.Hkv):

@@ -16,12 +16,13 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
 def _problem(seed, B=1, Nq=40, Nk=40, Hq=2, Hkv=1, d=8, causal=True, mask="dense", bias=True, density=0.5,
-             scale=None, keep_diag=False):
+             scale=None, keep_diag=False, dv=None):
     g = torch.Generator().manual_seed(seed)
+    dv = d if dv is None else dv
     q = torch.randn(B, Nq, Hq, d, generator=g, dtype=torch.float64)
     k = torch.randn(B, Nk, Hkv, d, generator=g, dtype=torch.float64)
-    v = torch.randn(B, Nk, Hkv, d, generator=g, dtype=torch.float64)
-    do = torch.randn(B, Nq, Hq, d, generator=g, dtype=torch.float64)
+    v = torch.randn(B, Nk, Hkv, dv, generator=g, dtype=torch.float64)
+    do = torch.randn(B, Nq, Hq, dv, generator=g, dtype=torch.float64)
     bb = torch.randn(B, Hkv, Nq, Nk, generator=g, dtype=torch.float64) if bias else None
     m = cr = None
     if mask == "dense":
@@ -85,11 +86,14 @@ def _sdpa(p):
             k.grad.permute(0, 2, 1, 3).numpy(), v.grad.permute(0, 2, 1, 3).numpy(), bias.grad.numpy())
 
 
-@pytest.mark.parametrize("Hq,Hkv,causal,with_mask", [(2, 1, True, True), (4, 2, False, True), (4, 4, True, False),
-                                                     (6, 2, True, True)])
-def test_matches_torch_sdpa(Hq, Hkv, causal, with_mask):
+@pytest.mark.parametrize("Hq,Hkv,causal,with_mask,dv", [(2, 1, True, True, 16), (4, 2, False, True, 16),
+                                                        (4, 4, True, False, 16), (6, 2, True, True, 16),
+                                                        (4, 2, True, True, 24), (2, 1, False, True, 8)])
+def test_matches_torch_sdpa(Hq, Hkv, causal, with_mask, dv):
+    """Against torch's SDPA, also with a V head dim other than the Q/K one (dv = 24 and 8 with
+    d = 16, as the 192 / 128 configuration of the FlashMask README head-dim table)."""
     p = _problem(11, B=2, Nq=70, Nk=70, Hq=Hq, Hkv=Hkv, d=16, causal=causal,
-                 mask="dense" if with_mask else None, density=0.6, keep_diag=True, scale=0.3)
+                 mask="dense" if with_mask else None, density=0.6, keep_diag=True, scale=0.3, dv=dv)
     O, _ = orc.forward(p)
     dq, dk, dv, dbias = orc.backward(p)
     rO, rdq, rdk, rdv, rdb = _sdpa(p)
