@@ -52,7 +52,8 @@ int validate(const fdma_args* a, bool need_workspace) {
   if (a == nullptr) return FDMA_ERR_INVALID;
   if (a->B <= 0 || a->Nq <= 0 || a->Nk <= 0 || a->Hq <= 0 || a->Hkv <= 0) return FDMA_ERR_INVALID;
   if (a->Hq % a->Hkv != 0) return FDMA_ERR_INVALID;
-  if (!head_dim_ok(a->d)) return FDMA_ERR_UNSUPPORTED;
+  if (a->dv < 0) return FDMA_ERR_INVALID;
+  if (!fwd_head_dims_ok(a->d, head_dim_v(*a))) return FDMA_ERR_UNSUPPORTED;
   if (cdiv(a->Nk, kTile) > kMaxKTiles || cdiv(a->Nq, kTile) > kMaxKTiles) return FDMA_ERR_UNSUPPORTED;
   if (!(std::isfinite(a->scale) && a->scale > 0.f)) return FDMA_ERR_INVALID;
   if (a->is_causal < 0 || a->is_causal > 2) return FDMA_ERR_INVALID;
@@ -200,7 +201,8 @@ extern "C" {
 
 size_t fdma_workspace_size(const fdma_args* a, int for_bwd) {
   if (a == nullptr || a->B <= 0 || a->Nq <= 0 || a->Nk <= 0 || a->Hq <= 0 || a->Hkv <= 0 || a->Hq % a->Hkv ||
-      !head_dim_ok(a->d))
+      a->dv < 0 ||
+      !(for_bwd ? bwd_head_dims_ok(a->d, head_dim_v(*a)) : fwd_head_dims_ok(a->d, head_dim_v(*a))))
     return 0;
   const WorkspaceLayout w = workspace_layout(a->B, a->Nq, a->Nk, a->Hq, a->Hkv, a->d);
   return for_bwd ? w.total_bwd : w.total_fwd;
@@ -230,9 +232,10 @@ int fdma_fwd(const fdma_args* a, void* out, float* lse, void* stream_v) {
   const WorkspaceLayout w = workspace_layout(a->B, a->Nq, a->Nk, a->Hq, a->Hkv, a->d);
   uint8_t* ws = static_cast<uint8_t*>(a->workspace);
   CUtensorMap tq, tk, tv, tb;
+  const int dv = head_dim_v(*a);
   if (!bshd_map(&tq, a->q, a->B, a->Nq, a->Hq, a->d, a->q_stride) ||
       !bshd_map(&tk, a->k, a->B, a->Nk, a->Hkv, a->d, a->k_stride) ||
-      !bshd_map(&tv, a->v, a->B, a->Nk, a->Hkv, a->d, a->v_stride))
+      !bshd_map(&tv, a->v, a->B, a->Nk, a->Hkv, dv, a->v_stride))
     return FDMA_ERR_UNSUPPORTED;
   const bool has_bias = a->bias != nullptr;
   if (has_bias) {
@@ -248,6 +251,7 @@ int fdma_fwd(const fdma_args* a, void* out, float* lse, void* stream_v) {
   p.Hkv = a->Hkv;
   p.G = a->Hq / a->Hkv;
   p.d = a->d;
+  p.dv = dv;
   p.nTq = cdiv(a->Nq, kTile);
   p.nTk = cdiv(a->Nk, kTile);
   p.scale = a->scale;
@@ -260,13 +264,22 @@ int fdma_fwd(const fdma_args* a, void* out, float* lse, void* stream_v) {
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
   p.err = err;
-  return launch_fwd(padded_head_dim(a->d), has_bias, tq, tk, tv, tb, p, stream) == cudaSuccess ? FDMA_OK
+  // up to 128 the kernels run on the padded width (64 or 128) with the missing columns read
+  // as zeros; 192 / 128 and 256 / 256 run on the wide kernel at their own widths
+  const int run_d = a->d <= 128 ? padded_head_dim(a->d) : a->d;
+  const int run_dv = a->d <= 128 ? run_d : dv;
+  return launch_fwd(run_d, run_dv, has_bias, tq, tk, tv, tb, p, stream) == cudaSuccess ? FDMA_OK
                                                                                                : FDMA_ERR_CUDA;
 }
 
 int fdma_bwd(const fdma_args* a, const void* out, const void* dout, const float* lse, void* dq, void* dk, void* dv,
              void* dbias, void* stream_v) {
-  int st = validate(a, true);
+  int st = validate(a, false);
+  if (st != FDMA_OK) return st;
+  // forward-only head dims are refused before the workspace is looked at (fdma_workspace_size
+  // has no backward size for them)
+  if (!bwd_head_dims_ok(a->d, head_dim_v(*a))) return FDMA_ERR_UNSUPPORTED;
+  st = validate(a, true);
   if (st != FDMA_OK) return st;
   if (out == nullptr || dout == nullptr || lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
     return FDMA_ERR_INVALID;

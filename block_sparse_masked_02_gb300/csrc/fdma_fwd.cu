@@ -7,8 +7,9 @@
 //
 // One CTA = one (batch, query head, 128-row query tile).  Six warps:
 //   warp 0      TMA producer: Q once, then K, V and the 128x128 bias tile of
-//               every ACTIVE key tile into two-deep rings (skipped tiles are
-//               never requested);
+//               every ACTIVE key tile into rings (skipped tiles are never
+//               requested): two slots each, or one where a 192- or 256-wide
+//               tile leaves no room for two in shared memory;
 //   warp 1      TMEM owner and single-thread tcgen05.mma issuer:
 //               S_n = Q K_n^T (SS, fp32 in TMEM, double-buffered), then
 //               O += P_{n-1} V_{n-1} with P read from TMEM (TS);
@@ -16,7 +17,9 @@
 //               mask bits on partial tiles, online max/sum with lazy O
 //               rescaling, P written back to TMEM as packed bf16; final
 //               O / l and lse.
-// TMEM columns: S[0] 0..127, S[1] 128..255, O 256..256+d.
+// TMEM columns: S[0] 0..127, S[1] 128..255, O 256..256+dv.
+// Head dims: q/k width DQK and v/out width DV are 64 or 128 (equal), or 192 / 128
+// and 256 / 256 (FlashMask README, "Performance", SM100 head-dim table).
 #include "fdma_internal.h"
 #include "fdma_ptx.cuh"
 
@@ -51,18 +54,26 @@ enum FwdBar : int {
   kNumFwdBars = 21
 };
 
-template <int D, bool HAS_BIAS>
+template <int DQK, int DV, bool HAS_BIAS>
 struct FwdSmem {
-  static constexpr uint32_t kQB = 128u * D * 2u;  // one Q/K/V tile (bf16)
+  static constexpr uint32_t kQB = 128u * DQK * 2u;  // one Q or K tile (bf16)
+  static constexpr uint32_t kVB = 128u * DV * 2u;   // one V tile
   static constexpr uint32_t kBB = 128u * 128u * 2u;
+  static constexpr int kKS = DQK <= 128 ? 2 : 1;  // K ring slots
+  static constexpr int kVS = DV <= 128 ? 2 : 1;   // V ring slots
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffK = kQB;
-  static constexpr uint32_t kOffV = kOffK + 2 * kQB;
-  static constexpr uint32_t kOffBias = kOffV + 2 * kQB;
-  static constexpr uint32_t kOffBar = kOffBias + (HAS_BIAS ? 2 * kBB : 0u);
+  static constexpr uint32_t kOffV = kOffK + kKS * kQB;
+  static constexpr uint32_t kOffBias = kOffV + kVS * kVB;
+  static constexpr uint32_t kTail = kNumFwdBars * 8 + kMaxKTiles + 16;  // barriers, map row, misc
+  // bias ring slots: two where they fit in the 227 KB a CTA may use, else one
+  static constexpr int kBS = !HAS_BIAS ? 0 : (kOffBias + 2 * kBB + kTail <= 232448u ? 2 : 1);
+  static constexpr int kBSlots = kBS > 0 ? kBS : 1;  // (for slot arithmetic without a bias)
+  static constexpr uint32_t kOffBar = kOffBias + kBS * kBB;
   static constexpr uint32_t kOffMap = kOffBar + kNumFwdBars * 8;
   static constexpr uint32_t kOffMisc = kOffMap + kMaxKTiles;
   static constexpr uint32_t kTotal = kOffMisc + 16;
+  static_assert(kTotal <= 232448u, "forward shared memory exceeds the per-CTA limit");
 };
 
 __device__ __forceinline__ int next_active(const int8_t* row, int kt, int n) {
@@ -78,15 +89,17 @@ __device__ __forceinline__ uint64_t kmajor_step(int k, uint32_t rows) {
   return static_cast<uint64_t>(((k >> 2) * rows * 128u + (k & 3) * 32u) >> 4);
 }
 
-template <int D, bool HAS_BIAS>
+template <int DQK, int DV, bool HAS_BIAS>
 __global__ void __launch_bounds__(192, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmB,
                const FwdParams p) {
-  using L = FwdSmem<D, HAS_BIAS>;
-  constexpr int KB = D / 64;  // 64-column swizzle blocks along the head dim
+  using L = FwdSmem<DQK, DV, HAS_BIAS>;
+  constexpr int KB = DQK / 64;  // 64-column swizzle blocks along the q/k head dim
+  constexpr int VB = DV / 64;   // ... along the v head dim
+  constexpr int KS = L::kKS, VS = L::kVS, BS = L::kBSlots;
   constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
-  constexpr uint32_t IDESC_O = idesc_bf16(128, D, false, true);
+  constexpr uint32_t IDESC_O = idesc_bf16(128, DV, false, true);
 
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
@@ -150,40 +163,43 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
       for (int c = 0; c < KB; ++c) tma_load_4d(sQ + c * 16384, &tmQ, &bars[kQFull], c * 64, q0, h, b);
       int n = 0;
-      int issued = 0;
+      int nk = 0, nb = 0, nv = 0;  // fills issued into the K, bias and V rings
       for (int kt = first_kt; kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
-        const int s = n & 1;
-        const uint32_t ph = ((n >> 1) & 1) ^ 1;
         const int k0 = kt * kTile;
-        if (!mbar_wait(&bars[kKEmpty + s], ph, p.err, kDevErrTimeout, abort_flag)) break;
-        mbar_arrive_expect_tx(&bars[kKFull + s], L::kQB);
+        const int sk = n % KS, sb = n % BS, sv = n % VS;
+        if (!mbar_wait(&bars[kKEmpty + sk], ((n / KS) & 1) ^ 1, p.err, kDevErrTimeout, abort_flag)) break;
+        mbar_arrive_expect_tx(&bars[kKFull + sk], L::kQB);
 #pragma unroll
         for (int c = 0; c < KB; ++c)
-          tma_load_4d(sK + s * L::kQB + c * 16384, &tmK, &bars[kKFull + s], c * 64, k0, g, b);
+          tma_load_4d(sK + sk * L::kQB + c * 16384, &tmK, &bars[kKFull + sk], c * 64, k0, g, b);
+        nk = n + 1;
         if (HAS_BIAS) {
-          if (!mbar_wait(&bars[kBEmpty + s], ph, p.err, kDevErrTimeout, abort_flag)) break;
-          mbar_arrive_expect_tx(&bars[kBFull + s], L::kBB);
+          if (!mbar_wait(&bars[kBEmpty + sb], ((n / BS) & 1) ^ 1, p.err, kDevErrTimeout, abort_flag)) break;
+          mbar_arrive_expect_tx(&bars[kBFull + sb], L::kBB);
 #pragma unroll
           for (int c = 0; c < 2; ++c)
-            tma_load_4d_hint(sB + s * L::kBB + c * 16384, &tmB, &bars[kBFull + s], k0 + c * 64, q0, g * p.bias_hsel,
-                             b * p.bias_bsel, bias_pol);
+            tma_load_4d_hint(sB + sb * L::kBB + c * 16384, &tmB, &bars[kBFull + sb], k0 + c * 64, q0,
+                             g * p.bias_hsel, b * p.bias_bsel, bias_pol);
+          nb = n + 1;
         }
-        if (!mbar_wait(&bars[kVEmpty + s], ph, p.err, kDevErrTimeout, abort_flag)) break;
-        mbar_arrive_expect_tx(&bars[kVFull + s], L::kQB);
+        if (!mbar_wait(&bars[kVEmpty + sv], ((n / VS) & 1) ^ 1, p.err, kDevErrTimeout, abort_flag)) break;
+        mbar_arrive_expect_tx(&bars[kVFull + sv], L::kVB);
 #pragma unroll
-        for (int c = 0; c < KB; ++c)
-          tma_load_4d(sV + s * L::kQB + c * 16384, &tmV, &bars[kVFull + s], c * 64, k0, g, b);
-        issued = n + 1;
+        for (int c = 0; c < VB; ++c)
+          tma_load_4d(sV + sv * L::kVB + c * 16384, &tmV, &bars[kVFull + sv], c * 64, k0, g, b);
+        nv = n + 1;
       }
       if (*abort_flag) {
-        // let our own copies land before the CTA retires
+        // let our own copies land before the CTA retires: in each ring only the last fill
+        // of every slot can still be in flight (earlier ones were consumed before the slot
+        // was refilled)
         mbar_wait(&bars[kQFull], 0, p.err, kDevErrTimeout, nullptr);
-        for (int m = issued > 2 ? issued - 2 : 0; m < issued; ++m) {
-          const uint32_t ph = (m >> 1) & 1;
-          mbar_wait(&bars[kKFull + (m & 1)], ph, p.err, kDevErrTimeout, nullptr);
-          mbar_wait(&bars[kVFull + (m & 1)], ph, p.err, kDevErrTimeout, nullptr);
-          if (HAS_BIAS) mbar_wait(&bars[kBFull + (m & 1)], ph, p.err, kDevErrTimeout, nullptr);
-        }
+        for (int m = nk > KS ? nk - KS : 0; m < nk; ++m)
+          mbar_wait(&bars[kKFull + m % KS], (m / KS) & 1, p.err, kDevErrTimeout, nullptr);
+        for (int m = nv > VS ? nv - VS : 0; m < nv; ++m)
+          mbar_wait(&bars[kVFull + m % VS], (m / VS) & 1, p.err, kDevErrTimeout, nullptr);
+        for (int m = nb > BS ? nb - BS : 0; m < nb; ++m)
+          mbar_wait(&bars[kBFull + m % BS], (m / BS) & 1, p.err, kDevErrTimeout, nullptr);
       }
     }
   } else if (warp == 1) {
@@ -193,48 +209,34 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const uint64_t qdesc = sdesc_sw128(smem_u32(sQ), 16, 1024);
       int n = 0;
-      for (int kt = first_kt; ok && kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
-        const int s = n & 1;
-        const uint32_t ph = (n >> 1) & 1;
-        if (!(ok = mbar_wait(&bars[kKFull + s], ph, p.err, kDevErrTimeout, abort_flag))) break;
+      // O += P_m V_m: P from TMEM slot m & 1, V from ring slot m % VS
+      auto issue_pv = [&](int m) -> bool {
+        const int sm = m & 1, sv = m % VS;
+        if (!mbar_wait(&bars[kVFull + sv], (m / VS) & 1, p.err, kDevErrTimeout, abort_flag)) return false;
+        if (!mbar_wait(&bars[kPReady + sm], (m >> 1) & 1, p.err, kDevErrTimeout, abort_flag)) return false;
         tc_fence_after();
-        const uint64_t kdesc = sdesc_sw128(smem_u32(sK + s * L::kQB), 16, 1024);
+        const uint64_t vdesc = sdesc_sw128(smem_u32(sV + sv * L::kVB), 16384, 1024);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
+        for (int k = 0; k < 8; ++k)
+          umma_ts(tbase + 256, tbase + sm * 128 + k * 8, vdesc + static_cast<uint64_t>((k * 2048) >> 4), IDESC_O,
+                  (m > 0 || k > 0) ? 1u : 0u);
+        umma_commit(&bars[kVEmpty + sv]);
+        umma_commit(&bars[kODone]);
+        return true;
+      };
+      for (int kt = first_kt; ok && kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
+        const int s = n & 1, sk = n % KS;
+        if (!(ok = mbar_wait(&bars[kKFull + sk], (n / KS) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        tc_fence_after();
+        const uint64_t kdesc = sdesc_sw128(smem_u32(sK + sk * L::kQB), 16, 1024);
+#pragma unroll
+        for (int k = 0; k < DQK / 16; ++k)
           umma_ss(tbase + s * 128, qdesc + kmajor_step(k, 128), kdesc + kmajor_step(k, 128), IDESC_S, k > 0);
         umma_commit(&bars[kSFull + s]);
-        umma_commit(&bars[kKEmpty + s]);
-        if (n > 0) {
-          const int m = n - 1, sm = m & 1;
-          const uint32_t pm = (m >> 1) & 1;
-          if (!(ok = mbar_wait(&bars[kVFull + sm], pm, p.err, kDevErrTimeout, abort_flag))) break;
-          if (!(ok = mbar_wait(&bars[kPReady + sm], pm, p.err, kDevErrTimeout, abort_flag))) break;
-          tc_fence_after();
-          const uint64_t vdesc = sdesc_sw128(smem_u32(sV + sm * L::kQB), 16384, 1024);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            umma_ts(tbase + 256, tbase + sm * 128 + k * 8, vdesc + static_cast<uint64_t>((k * 2048) >> 4), IDESC_O,
-                    (m > 0 || k > 0) ? 1u : 0u);
-          umma_commit(&bars[kVEmpty + sm]);
-          umma_commit(&bars[kODone]);
-        }
+        umma_commit(&bars[kKEmpty + sk]);
+        if (n > 0 && !(ok = issue_pv(n - 1))) break;
       }
-      if (ok && n > 0) {
-        const int m = n - 1, sm = m & 1;
-        const uint32_t pm = (m >> 1) & 1;
-        ok = mbar_wait(&bars[kVFull + sm], pm, p.err, kDevErrTimeout, abort_flag) &&
-             mbar_wait(&bars[kPReady + sm], pm, p.err, kDevErrTimeout, abort_flag);
-        if (ok) {
-          tc_fence_after();
-          const uint64_t vdesc = sdesc_sw128(smem_u32(sV + sm * L::kQB), 16384, 1024);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            umma_ts(tbase + 256, tbase + sm * 128 + k * 8, vdesc + static_cast<uint64_t>((k * 2048) >> 4), IDESC_O,
-                    (m > 0 || k > 0) ? 1u : 0u);
-          umma_commit(&bars[kVEmpty + sm]);
-          umma_commit(&bars[kODone]);
-        }
-      }
+      if (ok && n > 0) ok = issue_pv(n - 1);
       umma_commit(&bars[kOFinal]);
       umma_commit(&bars[kDrain]);
       mbar_wait(&bars[kDrain], 0, p.err, kDevErrTimeout, nullptr);
@@ -268,8 +270,9 @@ __global__ void __launch_bounds__(192, 1)
         for (int j = 0; j < 32; ++j) x[c * 32 + j] = __uint_as_float(raw[j]) * p.scale_log2;
       }
       if (HAS_BIAS) {
-        if (!(ok = mbar_wait(&bars[kBFull + s], ph, p.err, kDevErrTimeout, abort_flag))) break;
-        const uint8_t* bt = sB + s * L::kBB + r * 128;
+        const int sb = n % BS;
+        if (!(ok = mbar_wait(&bars[kBFull + sb], (n / BS) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        const uint8_t* bt = sB + sb * L::kBB + r * 128;
 #pragma unroll
         for (int cc = 0; cc < 16; ++cc) {
           const uint4 v = *reinterpret_cast<const uint4*>(bt + (cc >> 3) * 16384 + (((cc & 7) ^ (r & 7)) << 4));
@@ -281,7 +284,7 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
         fence_proxy_async_smem();  // generic reads of the slot before its next TMA write
-        mbar_arrive(&bars[kBEmpty + s]);
+        mbar_arrive(&bars[kBEmpty + sb]);
       }
       if (partial) {
         const uint32_t bw[4] = {bits.x, bits.y, bits.z, bits.w};
@@ -314,7 +317,7 @@ __global__ void __launch_bounds__(192, 1)
         if (!(ok = mbar_wait(&bars[kODone], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < DV / 32; ++c) {
           tmem_ld32(tl + 256 + c * 32, raw);
           tmem_ld_wait(raw);
           uint32_t lo[16], hi[16];
@@ -354,9 +357,9 @@ __global__ void __launch_bounds__(192, 1)
     if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint16_t* orow = p.out + ((static_cast<int64_t>(b) * p.Nq + i) * p.Hq + h) * p.d;
+      uint16_t* orow = p.out + ((static_cast<int64_t>(b) * p.Nq + i) * p.Hq + h) * p.dv;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < DV / 32; ++c) {
         if (n > 0) {
           tmem_ld32(tl + 256 + c * 32, raw);
           tmem_ld_wait(raw);
@@ -372,7 +375,7 @@ __global__ void __launch_bounds__(192, 1)
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int v = 0; v < 4; ++v)
-            if (c * 32 + v * 8 < p.d) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            if (c * 32 + v * 8 < p.dv) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
       if (i < p.Nq)
@@ -777,7 +780,7 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
     if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint16_t* orow = p.out + ((static_cast<int64_t>(b) * p.Nq + i) * p.Hq + h) * p.d;
+      uint16_t* orow = p.out + ((static_cast<int64_t>(b) * p.Nq + i) * p.Hq + h) * p.dv;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         if (n > 0) {
@@ -795,7 +798,7 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int v = 0; v < 4; ++v)
-            if (c * 32 + v * 8 < p.d) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            if (c * 32 + v * 8 < p.dv) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
       if (i < p.Nq)
@@ -827,11 +830,11 @@ cudaError_t launch_fwd2_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   return cudaGetLastError();
 }
 
-template <int D, bool HB>
+template <int DQK, int DV, bool HB>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tb,
                          const FwdParams& p, cudaStream_t stream) {
-  using L = FwdSmem<D, HB>;
-  auto kern = fwd_kernel<D, HB>;
+  using L = FwdSmem<DQK, DV, HB>;
+  auto kern = fwd_kernel<DQK, DV, HB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.B) * p.Hq * p.nTq;
@@ -841,18 +844,25 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 }  // namespace
 
-cudaError_t launch_fwd(int d, bool has_bias, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tb, const FwdParams& p, cudaStream_t stream) {
+cudaError_t launch_fwd(int d, int dv, bool has_bias, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& tb, const FwdParams& p, cudaStream_t stream) {
+  if (d == 192 && dv == 128)
+    return has_bias ? launch_fwd_t<192, 128, true>(tq, tk, tv, tb, p, stream)
+                    : launch_fwd_t<192, 128, false>(tq, tk, tv, tb, p, stream);
+  if (d == 256 && dv == 256)
+    return has_bias ? launch_fwd_t<256, 256, true>(tq, tk, tv, tb, p, stream)
+                    : launch_fwd_t<256, 256, false>(tq, tk, tv, tb, p, stream);
+  if (dv != d) return cudaErrorInvalidValue;
   if (p.G % 2 == 0) {
     if (d == 128) return has_bias ? launch_fwd2_t<128, true>(tq, tk, tv, tb, p, stream)
                                   : launch_fwd2_t<128, false>(tq, tk, tv, tb, p, stream);
     if (d == 64) return has_bias ? launch_fwd2_t<64, true>(tq, tk, tv, tb, p, stream)
                                  : launch_fwd2_t<64, false>(tq, tk, tv, tb, p, stream);
   }
-  if (d == 128) return has_bias ? launch_fwd_t<128, true>(tq, tk, tv, tb, p, stream)
-                                : launch_fwd_t<128, false>(tq, tk, tv, tb, p, stream);
-  if (d == 64) return has_bias ? launch_fwd_t<64, true>(tq, tk, tv, tb, p, stream)
-                               : launch_fwd_t<64, false>(tq, tk, tv, tb, p, stream);
+  if (d == 128) return has_bias ? launch_fwd_t<128, 128, true>(tq, tk, tv, tb, p, stream)
+                                : launch_fwd_t<128, 128, false>(tq, tk, tv, tb, p, stream);
+  if (d == 64) return has_bias ? launch_fwd_t<64, 64, true>(tq, tk, tv, tb, p, stream)
+                               : launch_fwd_t<64, 64, false>(tq, tk, tv, tb, p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -25,6 +25,14 @@ inline int padded_head_dim(int d) { return d <= 64 ? 64 : 128; }
 // head dim runs on the next one up, the missing columns of Q, K, V and dO read as zeros by TMA
 // (out-of-range fill) and the padding columns of the results never stored.
 inline bool head_dim_ok(int d) { return d >= 8 && d <= 128 && d % 8 == 0; }
+// Head dim of v, out and dout: fdma_args.dv, 0 meaning the q/k head dim d.
+inline int head_dim_v(const fdma_args& a) { return a.dv > 0 ? a.dv : a.d; }
+// Forward: d = dv from 8 to 128 (the 64- / 128-wide kernels), or (d, dv) = (192, 128) or
+// (256, 256) on the wide single-head kernel.  The backward takes d = dv up to 128 only.
+inline bool fwd_head_dims_ok(int d, int dv) {
+  return (head_dim_ok(d) && dv == d) || (d == 192 && dv == 128) || (d == 256 && dv == 256);
+}
+inline bool bwd_head_dims_ok(int d, int dv) { return head_dim_ok(d) && dv == d; }
 constexpr int kSkip = 0, kPartial = 1, kFull = 2;
 
 // Device error word values (first writer wins).
@@ -51,7 +59,8 @@ struct ClassifyParams {
 
 struct FwdParams {
   int B, Nq, Nk, Hq, Hkv, G, nTq, nTk;
-  int d;  // head dim of q, k, v, out (the kernel runs on its padded width, 64 or 128)
+  int d;   // head dim of q, k (up to 128 the kernel runs on its padded width, 64 or 128)
+  int dv;  // head dim of v, out (= d up to 128)
   int bias_bsel, bias_hsel;  // 0 where the bias is broadcast over batch / kv head (TMA coordinate 0)
   float scale, scale_log2;  // softmax scale and scale * log2(e)
   int test_short_wait;      // FDMA_FLAG_TEST_SHORT_WAIT: the softmax warps time out on purpose
@@ -130,7 +139,7 @@ struct TopkParams {
 cudaError_t launch_classify(const ClassifyParams& p, cudaStream_t stream);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
 size_t topk_smem_bytes(int Nk);
-cudaError_t launch_fwd(int d, bool has_bias, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_fwd(int d, int dv, bool has_bias, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tb, const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream);
 cudaError_t launch_bwd(int d, bool has_bias, bool want_dbias, const CUtensorMap& tq, const CUtensorMap& tk,

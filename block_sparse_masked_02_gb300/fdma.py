@@ -52,7 +52,7 @@ class FdmaArgs(ctypes.Structure):
         ("bias", ctypes.c_void_p), ("bias_stride", ctypes.c_int64 * 3),
         ("is_causal", ctypes.c_int32), ("scale", ctypes.c_float), ("flags", ctypes.c_uint32),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-        ("q_offset", ctypes.c_int32),
+        ("q_offset", ctypes.c_int32), ("dv", ctypes.c_int32),
     ]
 
 
@@ -148,8 +148,8 @@ def pack_mask(mask: torch.Tensor) -> PackedMask:
 
 def make_args(q, k, v, *, mask=None, colranges=None, bias=None, causal=False, scale=None, workspace=None,
               flags=0, causal_offset=None) -> FdmaArgs:
-    """Fill fdma_args from tensors: q (B,Nq,Hq,d), k/v (B,Nk,Hkv,d) with a contiguous
-    head dim; mask (B,Hkv,Nq,Nk) bf16, uint8 or bool and bias (B,Hkv,Nq,Nk) bf16 with
+    """Fill fdma_args from tensors: q (B,Nq,Hq,d), k (B,Nk,Hkv,d), v (B,Nk,Hkv,dv) with a
+    contiguous head dim (dv = d, or the forward-only pairs 192 / 128 and 256 / 256); mask (B,Hkv,Nq,Nk) bf16, uint8 or bool and bias (B,Hkv,Nq,Nk) bf16 with
     contiguous columns (stride 0 broadcasts a batch or head axis); colranges int32
     (B,Hkv,Nk,2) (one masked row range per key) or (B,Hkv,Nk,4) (two).  causal=True keeps
     keys j <= i + (Nk - Nq); with causal_offset=c (an int) keys j <= i + c instead, i.e. the
@@ -157,6 +157,7 @@ def make_args(q, k, v, *, mask=None, colranges=None, bias=None, causal=False, sc
     a = FdmaArgs()
     a.B, a.Nq, a.Hq, a.d = (int(x) for x in q.shape)
     a.Nk, a.Hkv = int(k.shape[1]), int(k.shape[2])
+    a.dv = int(v.shape[3])
     for name, t in (("q", q), ("k", k), ("v", v)):
         if t.dtype != torch.bfloat16 or t.stride(3) != 1:
             raise ValueError(f"{name} must be bf16 with a contiguous head dim")
@@ -212,7 +213,9 @@ def alloc_workspace(args: FdmaArgs, for_bwd: bool, device) -> torch.Tensor:
     n = workspace_size(args, for_bwd)
     if n == 0:
         # invalid shape: let the entry point name the problem (no workspace attached)
-        st = load().fdma_fwd(ctypes.byref(args), None, None, None)
+        lib = load()
+        st = lib.fdma_bwd(ctypes.byref(args), None, None, None, None, None, None, None, None) if for_bwd else \
+            lib.fdma_fwd(ctypes.byref(args), None, None, None)
         raise FdmaError(st if st != FDMA_OK else FDMA_ERR_INVALID, "fdma_workspace_size")
     ws = torch.empty(n + 256, dtype=torch.uint8, device=device)
     off = (-ws.data_ptr()) % 256
@@ -276,15 +279,15 @@ def topk_mask(bias, keep_window, *, mask_dtype=torch.bfloat16, fill_bias=True, i
 
 def fwd(q, k, v, *, mask=None, colranges=None, bias=None, causal=False, scale=None, workspace=None, flags=0,
         out=None, lse=None, stream=None, causal_offset=None):
-    """Returns (out (B,Nq,Hq,d) bf16, lse (B,Hq,Nq) fp32)."""
+    """Returns (out (B,Nq,Hq,dv) bf16, lse (B,Hq,Nq) fp32)."""
     _check_cuda(q, k, v, mask, colranges, bias, workspace)
     args = make_args(q, k, v, mask=mask, colranges=colranges, bias=bias, causal=causal, scale=scale, flags=flags,
                      causal_offset=causal_offset)
     ws = workspace if workspace is not None else alloc_workspace(args, False, q.device)
     _attach(args, ws)
-    B, Nq, Hq, d = q.shape
+    B, Nq, Hq, _ = q.shape
     if out is None:
-        out = torch.empty((B, Nq, Hq, d), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((B, Nq, Hq, v.shape[3]), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
     _raise(load().fdma_fwd(ctypes.byref(args), out.data_ptr(), lse.data_ptr(), _stream_ptr(stream)), "fdma_fwd")
@@ -328,9 +331,9 @@ def fwd_noalloc(q, k, v, *, mask=None, colranges=None, bias=None, causal=False, 
     _check_cuda(q, k, v, mask, colranges, bias)
     args = make_args(q, k, v, mask=mask, colranges=colranges, bias=bias, causal=causal, scale=scale, flags=flags,
                      causal_offset=causal_offset)
-    B, Nq, Hq, d = q.shape
+    B, Nq, Hq, _ = q.shape
     if out is None:
-        out = torch.empty((B, Nq, Hq, d), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((B, Nq, Hq, v.shape[3]), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
     _raise(load().fdma_fwd_noalloc(ctypes.byref(args), out.data_ptr(), lse.data_ptr(), _stream_ptr(stream)),

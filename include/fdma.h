@@ -85,13 +85,16 @@ typedef enum {
                                              failure path without any fault. */
 
 typedef struct fdma_args {
-  /* problem size: batch, query length, key length, query heads, kv heads, head dim (a multiple
-     of 8 from 8 to 128, run on the 64- or 128-wide kernels with the missing columns read as
-     zeros; other values: FDMA_ERR_UNSUPPORTED) */
+  /* problem size: batch, query length, key length, query heads, kv heads, head dim d of q and
+     k.  With dv (below) = d: a multiple of 8 from 8 to 128, run on the 64- or 128-wide kernels
+     with the missing columns read as zeros.  The forward also takes d = 192 with dv = 128 and
+     d = 256 with dv = 256 (FlashMask README, "Performance", SM100 head-dim table); fdma_bwd
+     returns FDMA_ERR_UNSUPPORTED for those.  Other values: FDMA_ERR_UNSUPPORTED. */
   int32_t B, Nq, Nk, Hq, Hkv, d;
 
-  /* q (B,Nq,Hq,d), k and v (B,Nk,Hkv,d); strides in ELEMENTS for (batch, seq, head); the
-     head-dim axis is contiguous.  seq/head/batch strides * 2 bytes must be multiples of 16. */
+  /* q (B,Nq,Hq,d), k (B,Nk,Hkv,d) and v (B,Nk,Hkv,dv); strides in ELEMENTS for (batch, seq,
+     head); the head-dim axis is contiguous.  seq/head/batch strides * 2 bytes must be multiples
+     of 16. */
   const void* q;
   int64_t q_stride[3];
   const void* k;
@@ -143,10 +146,15 @@ typedef struct fdma_args {
      parallelism: each rank's rows against all keys).  |q_offset| <= 2^30, else
      FDMA_ERR_INVALID.  Ignored for is_causal 0 and 1. */
   int32_t q_offset;
+
+  /* head dim of v, out and dout; 0 means dv = d (a zero-initialised struct keeps the equal
+     head dims).  Negative: FDMA_ERR_INVALID.  Allowed pairs: see d above. */
+  int32_t dv;
 } fdma_args;
 
 /* Bytes of workspace needed by fdma_classify_blocks / fdma_fwd (for_bwd = 0) or by
-   fdma_bwd as well (for_bwd = 1).  Returns 0 when the shape in args is invalid. */
+   fdma_bwd as well (for_bwd = 1).  Returns 0 when the shape in args is invalid,
+   or (for_bwd = 1) has forward-only head dims. */
 FDMA_API size_t fdma_workspace_size(const fdma_args* args, int for_bwd);
 
 /* Block classification (Flash-DMA "Key Features": OR-reduction over each
@@ -159,7 +167,7 @@ FDMA_API size_t fdma_workspace_size(const fdma_args* args, int for_bwd);
 FDMA_API int fdma_classify_blocks(const fdma_args* args, int block_m, int block_n, int8_t* block_map, void* stream);
 
 /* Forward.  Classifies (unless FDMA_FLAG_REUSE_CLASSIFICATION) and computes
-   out: bf16 (B,Nq,Hq,d) contiguous and lse: fp32 (B,Hq,Nq) contiguous.
+   out: bf16 (B,Nq,Hq,dv) contiguous and lse: fp32 (B,Hq,Nq) contiguous.
    Precision: the softmax weights enter the P V product rounded to bf16, and both O and lse
    are normalised by the sum of those rounded weights (so the weights that produced O sum to
    exactly 1).  lse is therefore the log-sum-exp of the definition up to a relative error of
@@ -167,7 +175,8 @@ FDMA_API int fdma_classify_blocks(const fdma_args* args, int block_m, int block_
    fdma_bwd expects this lse (it recomputes the same weights). */
 FDMA_API int fdma_fwd(const fdma_args* args, void* out, float* lse, void* stream);
 
-/* Backward.  out, dout: bf16 (B,Nq,Hq,d) contiguous; lse as written by fdma_fwd.
+/* Backward (head dims d = dv up to 128; FDMA_ERR_UNSUPPORTED for the forward-only 192 / 128
+   and 256 / 256).  out, dout: bf16 (B,Nq,Hq,d) contiguous; lse as written by fdma_fwd.
    Outputs dq: bf16 (B,Nq,Hq,d), dk and dv: bf16 (B,Nk,Hkv,d) (summed over each
    group's query heads), dbias: bf16 (B,Hkv,Nq,Nk) (NULL: not computed; requires
    args->bias != NULL), all contiguous.  Every dbias element is written (zeros in

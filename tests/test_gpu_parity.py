@@ -444,6 +444,44 @@ def test_small_head_dims(F, d, Hq, Hkv, kind):
     run_and_compare(F, inp, True, wl.scale, case=f"d{d}_hq{Hq}_hkv{Hkv}_{kind}")
 
 
+@pytest.mark.parametrize("d,dv,Hq,Hkv,kind,causal", [
+    (192, 128, 4, 2, "topk_bias", True), (192, 128, 3, 1, "colranges", True), (192, 128, 2, 2, "none", False),
+    (256, 256, 4, 2, "topk_bias", True), (256, 256, 2, 1, "colranges", True), (256, 256, 2, 2, "u8_bcast", False)])
+def test_wide_head_dims_forward(F, d, dv, Hq, Hkv, kind, causal):
+    """The head dims 192 / 128 and 256 / 256 of the FlashMask README SM100 table ("Performance")
+    run forward on the wide one-head kernel (one-slot K, V or bias rings where two do not fit in
+    shared memory): O (of width dv) and lse match the oracle, rows with no kept key give
+    lse = -inf and O = 0.  The backward refuses these head dims (FDMA_ERR_UNSUPPORTED)."""
+    N = 392  # three tiles and a ragged fourth
+    scale = 1.0 / math.sqrt(d)
+    if kind == "topk_bias":
+        wl = W.scaled(W.WORKLOADS["n4096_hq32_hkv8"], Nq=N, Nk=N, Hq=Hq, Hkv=Hkv, d=d, keep_window=110,
+                      seed=90 + d + Hq, scale=scale)
+    elif kind == "colranges":
+        wl = W.Workload("doc_wide_d", 1, N, N, Hq, Hkv, d, True, scale, "colranges", 0, False,
+                        doc_lo=60, doc_hi=180, seed=95 + d + Hq)
+    else:
+        wl = W.Workload("plain_wide_d", 2, N, N - 64, Hq, Hkv, d, False, scale, "none", 0, False, seed=97 + d)
+    inp = W.make_inputs(wl)
+    g = torch.Generator().manual_seed(1000 + d + dv)
+    inp["v"] = torch.randn(wl.B, wl.Nk, Hkv, dv, generator=g).bfloat16()
+    inp["dout"] = torch.randn(wl.B, wl.Nq, Hq, dv, generator=g).bfloat16()
+    if kind == "u8_bcast":
+        inp["mask"] = (torch.rand(wl.B, Hkv, wl.Nq, wl.Nk, generator=g) < 0.3).to(torch.uint8)
+        inp["mask"][:, :, 130:140] = 0  # rows with no kept key
+        inp["bias"] = torch.randn(1, Hkv, wl.Nq, wl.Nk, generator=g).bfloat16().expand(wl.B, Hkv, wl.Nq, wl.Nk)
+    run_and_compare(F, inp, causal, scale, check_bwd=False, case=f"fwd d{d}/dv{dv} hq{Hq} hkv{Hkv} {kind}")
+    q, k, v, do = (_cuda(inp[n]) for n in ("q", "k", "v", "dout"))
+    kw = dict(mask=_cuda(inp.get("mask")), colranges=_cuda(inp.get("colranges")), bias=_cuda(inp.get("bias")),
+              causal=causal, scale=scale)
+    out, lse = F.fwd(q, k, v, **kw)
+    assert out.shape == (wl.B, wl.Nq, Hq, dv)
+    with pytest.raises(F.FdmaError) as e:
+        F.bwd(q, k, v, out, do, lse, **kw)
+    assert e.value.status == F.FDMA_ERR_UNSUPPORTED
+    assert F.device_error() == 0
+
+
 def test_one_head_per_kv_head_with_bias(F):
     """G = 1 with a bias: the backward keeps one dO slot and reloads the bias buffer after each
     query tile's bias copy (no second dO slot to alternate with)."""
