@@ -16,7 +16,8 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libfdma.so")
-SOURCES = ["fdma_api.cu", "fdma_classify.cu", "fdma_fwd.cu", "fdma_bwd.cu", "fdma_noalloc.cu", "fdma_topk.cu"]
+SOURCES = ["fdma_api.cu", "fdma_classify.cu", "fdma_fwd.cu", "fdma_bwd.cu", "fdma_bwd_wide.cu", "fdma_noalloc.cu",
+           "fdma_topk.cu"]
 HEADERS = ["fdma_internal.h", "fdma_ptx.cuh", os.path.join("..", "..", "include", "fdma.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]

@@ -53,7 +53,7 @@ int validate(const fdma_args* a, bool need_workspace) {
   if (a->B <= 0 || a->Nq <= 0 || a->Nk <= 0 || a->Hq <= 0 || a->Hkv <= 0) return FDMA_ERR_INVALID;
   if (a->Hq % a->Hkv != 0) return FDMA_ERR_INVALID;
   if (a->dv < 0) return FDMA_ERR_INVALID;
-  if (!fwd_head_dims_ok(a->d, head_dim_v(*a))) return FDMA_ERR_UNSUPPORTED;
+  if (!head_dims_ok(a->d, head_dim_v(*a))) return FDMA_ERR_UNSUPPORTED;
   if (cdiv(a->Nk, kTile) > kMaxKTiles || cdiv(a->Nq, kTile) > kMaxKTiles) return FDMA_ERR_UNSUPPORTED;
   if (!(std::isfinite(a->scale) && a->scale > 0.f)) return FDMA_ERR_INVALID;
   if (a->is_causal < 0 || a->is_causal > 2) return FDMA_ERR_INVALID;
@@ -188,7 +188,7 @@ WorkspaceLayout workspace_layout(int B, int Nq, int Nk, int Hq, int Hkv, int d) 
   w.delta = off;
   off = align256(off + static_cast<size_t>(B) * Hq * nqpad * 4);
   w.dq_acc = off;
-  off = align256(off + static_cast<size_t>(B) * nqpad * Hq * padded_head_dim(d) * 4);
+  off = align256(off + static_cast<size_t>(B) * nqpad * Hq * dq_acc_width(d) * 4);
   w.total_bwd = off;
   return w;
 }
@@ -201,8 +201,7 @@ extern "C" {
 
 size_t fdma_workspace_size(const fdma_args* a, int for_bwd) {
   if (a == nullptr || a->B <= 0 || a->Nq <= 0 || a->Nk <= 0 || a->Hq <= 0 || a->Hkv <= 0 || a->Hq % a->Hkv ||
-      a->dv < 0 ||
-      !(for_bwd ? bwd_head_dims_ok(a->d, head_dim_v(*a)) : fwd_head_dims_ok(a->d, head_dim_v(*a))))
+      a->dv < 0 || !head_dims_ok(a->d, head_dim_v(*a)))
     return 0;
   const WorkspaceLayout w = workspace_layout(a->B, a->Nq, a->Nk, a->Hq, a->Hkv, a->d);
   return for_bwd ? w.total_bwd : w.total_fwd;
@@ -276,9 +275,6 @@ int fdma_bwd(const fdma_args* a, const void* out, const void* dout, const float*
              void* dbias, void* stream_v) {
   int st = validate(a, false);
   if (st != FDMA_OK) return st;
-  // forward-only head dims are refused before the workspace is looked at (fdma_workspace_size
-  // has no backward size for them)
-  if (!bwd_head_dims_ok(a->d, head_dim_v(*a))) return FDMA_ERR_UNSUPPORTED;
   st = validate(a, true);
   if (st != FDMA_OK) return st;
   if (out == nullptr || dout == nullptr || lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
@@ -301,12 +297,14 @@ int fdma_bwd(const fdma_args* a, const void* out, const void* dout, const float*
   const int nTq = cdiv(a->Nq, kTile), nTk = cdiv(a->Nk, kTile);
   const int nqpad = nTq * kTile;
 
+  const int dv_w = head_dim_v(*a);
+  const bool wide = a->d > 128;  // (192, 128) or (256, 256): the output-split kernels
   BwdPreParams pp{};
   pp.B = a->B;
   pp.Nq = a->Nq;
   pp.Hq = a->Hq;
-  pp.d = a->d;
-  pp.dpad = padded_head_dim(a->d);
+  pp.d = dv_w;  // delta = <dO, O> over the v head dim
+  pp.dpad = dq_acc_width(a->d);
   pp.nqpad = nqpad;
   pp.scale = a->scale;
   pp.out = static_cast<const uint16_t*>(out);
@@ -318,11 +316,11 @@ int fdma_bwd(const fdma_args* a, const void* out, const void* dout, const float*
   if (launch_bwd_pre(pp, stream) != cudaSuccess) return FDMA_ERR_CUDA;
 
   CUtensorMap tq, tk, tv, tdo;
-  const int64_t dstr[3] = {static_cast<int64_t>(a->Nq) * a->Hq * a->d, static_cast<int64_t>(a->Hq) * a->d, a->d};
+  const int64_t dstr[3] = {static_cast<int64_t>(a->Nq) * a->Hq * dv_w, static_cast<int64_t>(a->Hq) * dv_w, dv_w};
   if (!bshd_map(&tq, a->q, a->B, a->Nq, a->Hq, a->d, a->q_stride) ||
       !bshd_map(&tk, a->k, a->B, a->Nk, a->Hkv, a->d, a->k_stride) ||
-      !bshd_map(&tv, a->v, a->B, a->Nk, a->Hkv, a->d, a->v_stride) ||
-      !bshd_map(&tdo, dout, a->B, a->Nq, a->Hq, a->d, dstr))
+      !bshd_map(&tv, a->v, a->B, a->Nk, a->Hkv, dv_w, a->v_stride) ||
+      !bshd_map(&tdo, dout, a->B, a->Nq, a->Hq, dv_w, dstr))
     return FDMA_ERR_UNSUPPORTED;
   BwdParams p{};
   p.B = a->B;
@@ -365,15 +363,16 @@ int fdma_bwd(const fdma_args* a, const void* out, const void* dout, const float*
                             static_cast<uint64_t>(a->Hkv) * a->Nq * a->Nk * 2};
     if (!make_map(&tdb, dbias, dims, sb)) return FDMA_ERR_UNSUPPORTED;
   }
-  if (launch_bwd(padded_head_dim(a->d), a->bias != nullptr, dbias != nullptr, tq, tk, tv, tdo, tb, tdb, p, stream) !=
-      cudaSuccess)
-    return FDMA_ERR_CUDA;
+  const cudaError_t le =
+      wide ? launch_bwd_wide(a->d, dv_w, a->bias != nullptr, dbias != nullptr, tq, tk, tv, tdo, tb, p, stream)
+           : launch_bwd(padded_head_dim(a->d), a->bias != nullptr, dbias != nullptr, tq, tk, tv, tdo, tb, tdb, p, stream);
+  if (le != cudaSuccess) return FDMA_ERR_CUDA;
   DqConvertParams cp{};
   cp.B = a->B;
   cp.Nq = a->Nq;
   cp.Hq = a->Hq;
   cp.d = a->d;
-  cp.dpad = padded_head_dim(a->d);
+  cp.dpad = dq_acc_width(a->d);
   cp.nqpad = nqpad;
   cp.dq_acc = pp.dq_acc;
   cp.dq = static_cast<uint16_t*>(dq);

@@ -27,12 +27,13 @@ inline int padded_head_dim(int d) { return d <= 64 ? 64 : 128; }
 inline bool head_dim_ok(int d) { return d >= 8 && d <= 128 && d % 8 == 0; }
 // Head dim of v, out and dout: fdma_args.dv, 0 meaning the q/k head dim d.
 inline int head_dim_v(const fdma_args& a) { return a.dv > 0 ? a.dv : a.d; }
-// Forward: d = dv from 8 to 128 (the 64- / 128-wide kernels), or (d, dv) = (192, 128) or
-// (256, 256) on the wide single-head kernel.  The backward takes d = dv up to 128 only.
-inline bool fwd_head_dims_ok(int d, int dv) {
+// d = dv from 8 to 128 (the 64- / 128-wide kernels), or (d, dv) = (192, 128) or (256, 256)
+// (the wide one-head forward and the output-split backward).
+inline bool head_dims_ok(int d, int dv) {
   return (head_dim_ok(d) && dv == d) || (d == 192 && dv == 128) || (d == 256 && dv == 256);
 }
-inline bool bwd_head_dims_ok(int d, int dv) { return head_dim_ok(d) && dv == d; }
+// Row width of the fp32 dQ accumulator: the padded width up to 128, else d itself.
+inline int dq_acc_width(int d) { return d <= 128 ? padded_head_dim(d) : d; }
 constexpr int kSkip = 0, kPartial = 1, kFull = 2;
 
 // Device error word values (first writer wins).
@@ -142,6 +143,10 @@ size_t topk_smem_bytes(int Nk);
 cudaError_t launch_fwd(int d, int dv, bool has_bias, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tb, const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream);
+// (d, dv) = (192, 128) or (256, 256): both output parts, dBias from the first.
+cudaError_t launch_bwd_wide(int d, int dv, bool has_bias, bool want_dbias, const CUtensorMap& tq,
+                            const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                            const CUtensorMap& tb, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd(int d, bool has_bias, bool want_dbias, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tb, const CUtensorMap& tdb,
                        const BwdParams& p, cudaStream_t stream);

@@ -87,9 +87,10 @@ typedef enum {
 typedef struct fdma_args {
   /* problem size: batch, query length, key length, query heads, kv heads, head dim d of q and
      k.  With dv (below) = d: a multiple of 8 from 8 to 128, run on the 64- or 128-wide kernels
-     with the missing columns read as zeros.  The forward also takes d = 192 with dv = 128 and
-     d = 256 with dv = 256 (FlashMask README, "Performance", SM100 head-dim table); fdma_bwd
-     returns FDMA_ERR_UNSUPPORTED for those.  Other values: FDMA_ERR_UNSUPPORTED. */
+     with the missing columns read as zeros.  Also d = 192 with dv = 128 and d = 256 with
+     dv = 256 (FlashMask README, "Performance", SM100 head-dim table): the forward on a one-head
+     kernel, the backward on kernels that split the gradient columns into two parts (each
+     recomputes S and dP; slower per flop than d <= 128).  Other values: FDMA_ERR_UNSUPPORTED. */
   int32_t B, Nq, Nk, Hq, Hkv, d;
 
   /* q (B,Nq,Hq,d), k (B,Nk,Hkv,d) and v (B,Nk,Hkv,dv); strides in ELEMENTS for (batch, seq,
@@ -153,8 +154,7 @@ typedef struct fdma_args {
 } fdma_args;
 
 /* Bytes of workspace needed by fdma_classify_blocks / fdma_fwd (for_bwd = 0) or by
-   fdma_bwd as well (for_bwd = 1).  Returns 0 when the shape in args is invalid,
-   or (for_bwd = 1) has forward-only head dims. */
+   fdma_bwd as well (for_bwd = 1).  Returns 0 when the shape in args is invalid. */
 FDMA_API size_t fdma_workspace_size(const fdma_args* args, int for_bwd);
 
 /* Block classification (Flash-DMA "Key Features": OR-reduction over each
@@ -175,9 +175,8 @@ FDMA_API int fdma_classify_blocks(const fdma_args* args, int block_m, int block_
    fdma_bwd expects this lse (it recomputes the same weights). */
 FDMA_API int fdma_fwd(const fdma_args* args, void* out, float* lse, void* stream);
 
-/* Backward (head dims d = dv up to 128; FDMA_ERR_UNSUPPORTED for the forward-only 192 / 128
-   and 256 / 256).  out, dout: bf16 (B,Nq,Hq,d) contiguous; lse as written by fdma_fwd.
-   Outputs dq: bf16 (B,Nq,Hq,d), dk and dv: bf16 (B,Nk,Hkv,d) (summed over each
+/* Backward.  out, dout: bf16 (B,Nq,Hq,dv) contiguous; lse as written by fdma_fwd.
+   Outputs dq: bf16 (B,Nq,Hq,d), dk: bf16 (B,Nk,Hkv,d) and dv: bf16 (B,Nk,Hkv,dv) (summed over each
    group's query heads), dbias: bf16 (B,Hkv,Nq,Nk) (NULL: not computed; requires
    args->bias != NULL), all contiguous.  Every dbias element is written (zeros in
    skipped tiles and at masked positions).  Classifies unless

@@ -88,22 +88,23 @@ def test_argument_validation_before_any_cuda_call(F, field, value, status):
     assert rc == status
 
 
-@pytest.mark.parametrize("d,dv,fwd_ok", [(192, 128, True), (256, 0, True), (256, 256, True), (128, 64, False),
-                                         (192, 0, False), (192, 192, False), (256, 128, False), (64, 128, False)])
-def test_wide_head_dims_are_forward_only(F, d, dv, fwd_ok):
-    """(d, dv) = (192, 128) and (256, 256) have a forward workspace size and no backward one;
-    fdma_bwd refuses them with FDMA_ERR_UNSUPPORTED before any CUDA call.  Other unequal pairs
-    and other widths above 128 are refused by both."""
+@pytest.mark.parametrize("d,dv,ok", [(192, 128, True), (256, 0, True), (256, 256, True), (128, 64, False),
+                                     (192, 0, False), (192, 192, False), (256, 128, False), (64, 128, False)])
+def test_head_dim_pairs(F, d, dv, ok):
+    """(d, dv) = (192, 128) and (256, 256) have forward and backward workspace sizes (the
+    backward's fp32 dQ accumulator is d wide); other unequal pairs and other widths above 128
+    are refused by both entry points before any CUDA call."""
     a = _args(F, d=d, dv=dv)
     lib = F.load()
-    assert (lib.fdma_workspace_size(ctypes.byref(a), 0) > 0) == fwd_ok
-    assert lib.fdma_workspace_size(ctypes.byref(a), 1) == 0
-    fake = 1 << 20  # never dereferenced: the head dims are refused first, with or without a workspace
-    assert lib.fdma_bwd(ctypes.byref(a), fake, fake, fake, fake, fake, fake, None, None) == F.FDMA_ERR_UNSUPPORTED
-    a.workspace, a.workspace_bytes = 1 << 24, 1 << 30
-    assert lib.fdma_bwd(ctypes.byref(a), fake, fake, fake, fake, fake, fake, None, None) == F.FDMA_ERR_UNSUPPORTED
-    if not fwd_ok:
+    fw, bw = lib.fdma_workspace_size(ctypes.byref(a), 0), lib.fdma_workspace_size(ctypes.byref(a), 1)
+    assert (fw > 0) == ok and (bw > 0) == ok
+    if ok:
+        nqpad, Hq = 256, 4
+        assert bw - fw >= nqpad * Hq * d * 4  # the accumulator rows are d floats
+    else:
+        fake = 1 << 20  # never dereferenced: the head dims are refused first
         assert lib.fdma_fwd(ctypes.byref(a), fake, fake, None) == F.FDMA_ERR_UNSUPPORTED
+        assert lib.fdma_bwd(ctypes.byref(a), fake, fake, fake, fake, fake, fake, None, None) == F.FDMA_ERR_UNSUPPORTED
 
 
 def test_negative_v_head_dim_is_invalid(F):
