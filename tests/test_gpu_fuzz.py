@@ -34,7 +34,7 @@ def rel_l2(x, ref):
     return np.linalg.norm(x - ref) / (den if den > 0 else 1.0)
 
 
-def _case(seed):
+def _case(seed, wide=False):
     rng = np.random.default_rng(seed)
     g = torch.Generator().manual_seed(seed)
     B = int(rng.integers(1, 3))
@@ -42,6 +42,9 @@ def _case(seed):
     G = int(rng.integers(1, 5))
     Hq = G * Hkv
     d = 8 * int(rng.integers(1, 17))
+    dv = d
+    if wide:
+        d, dv = ((192, 128), (256, 256))[int(rng.integers(0, 2))]
     mask_kind = rng.choice(["none", "dense", "u8", "bits", "colranges", "colranges2"])
     bias_kind = rng.choice(["none", "full", "bcast_b", "bcast_h"])
     if mask_kind in ("dense", "u8") or bias_kind != "none":
@@ -57,7 +60,7 @@ def _case(seed):
     def bf(*shape):
         return torch.randn(*shape, generator=g).to(torch.bfloat16)
 
-    q, k, v, do = bf(B, Nq, Hq, d), bf(B, Nk, Hkv, d), bf(B, Nk, Hkv, d), bf(B, Nq, Hq, d)
+    q, k, v, do = bf(B, Nq, Hq, d), bf(B, Nk, Hkv, d), bf(B, Nk, Hkv, dv), bf(B, Nq, Hq, dv)
     bias = None
     if bias_kind == "full":
         bias = bf(B, Hkv, Nq, Nk)
@@ -87,9 +90,11 @@ def _case(seed):
                 want_dbias=want_dbias)
 
 
-@pytest.mark.parametrize("seed", list(range(1000, 1040)))
+@pytest.mark.parametrize("seed", list(range(1000, 1040)) + [("wide", s) for s in range(2000, 2012)])
 def test_random_problem_matches_oracle(F, seed):
-    c = _case(seed)
+    """Seeds 1000-1039: head dims 8..128; ("wide", 2000-2011): the head-dim pairs 192 / 128 and
+    256 / 256, with the other parameters drawn the same way."""
+    c = _case(seed[1], wide=True) if isinstance(seed, tuple) else _case(seed)
     cuda = lambda t: None if t is None else t.cuda()
     q, k, v, do = (cuda(c[n]) for n in ("q", "k", "v", "do"))
     bias = cuda(c["bias"])
