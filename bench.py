@@ -40,9 +40,9 @@ KERNELS_PER_STEP = 5  # classify, fwd, bwd_pre, bwd, dq_convert
 # DRAM bytes (read + write) of one bwd_kernel launch, per workload, from an ncu capture of
 # the current kernel; a workload without an entry reports null.  n16384_hq16_hkv4: one kv
 # group of the workload (Hq=4, Hkv=1) is captured; the four kv groups are independent CTAs
-# with the same work, so the full launch moves 4x that: 373,357,568 read and 534,967,808
+# with the same work, so the full launch moves 4x that: 373,442,048 read and 533,421,056
 # written per kv group.
-BWD_TRAFFIC_BYTES = {"n16384_hq16_hkv4": 4 * (373357568 + 534967808)}
+BWD_TRAFFIC_BYTES = {"n16384_hq16_hkv4": 4 * (373442048 + 533421056)}
 E2E_MAX_HOST_BYTES = 24e9  # larger workloads report no end-to-end number (pinned host copies)
 
 
