@@ -249,7 +249,10 @@ def run_gpu(args):
     ms_bwd = sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps
     err = fdma.device_error()
 
-    # ---- end to end: pinned host inputs in, results out, through the same C-ABI calls
+    # ---- end to end: pinned host inputs in, results out, through the same C-ABI calls.  Every
+    # step copies its own inputs in and its results out; the copies are pipelined across steps
+    # (two device slots; host->device on one stream, device->host on another), so step i+1's
+    # inputs arrive and step i-1's results leave while step i computes.
     names_in = [n for n in ("q", "k", "v", "dout", "mask", "colranges", "bias") if inp[n] is not None]
     dev_out = [t for t in (out, lse, *grads) if t is not None]
     h2d = sum(inp[n].numel() * inp[n].element_size() for n in names_in)
@@ -257,35 +260,60 @@ def run_gpu(args):
     e2e = None
     if h2d + d2h <= E2E_MAX_HOST_BYTES:
         host_in = {n: inp[n].cpu().pin_memory() for n in names_in}
-        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out]
-        e2e_steps = max(1, min(args.steps, 5))
-        dev_in = {n: torch.empty_like(inp[n]) for n in host_in}
+        slots = 2
+        dev_in = [{n: torch.empty_like(inp[n]) for n in host_in} for _ in range(slots)]
+        dev_res = [(torch.empty_like(out), torch.empty_like(lse), tuple(None if g is None else torch.empty_like(g)
+                                                                         for g in grads)) for _ in range(slots)]
+        host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out] for _ in range(slots)]
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(slots)]
+        ev_done = [torch.cuda.Event() for _ in range(slots)]
+        ev_out = [torch.cuda.Event() for _ in range(slots)]
+        e2e_steps = max(2, min(args.steps, 6))
 
-        def e2e_step():
-            for n, t in host_in.items():
-                dev_in[n].copy_(t, non_blocking=True)
-            ekw = dict(mask=dev_in.get("mask"), colranges=dev_in.get("colranges"), bias=dev_in.get("bias"),
+        def e2e_step(i):
+            sl = i % slots
+            din, (o_, l_, g_), hout = dev_in[sl], dev_res[sl], host_out[sl]
+            with torch.cuda.stream(s_in):
+                if i >= slots:
+                    s_in.wait_event(ev_done[sl])  # step i-2's compute has finished with this slot
+                for n, t in host_in.items():
+                    din[n].copy_(t, non_blocking=True)
+                ev_in[sl].record(s_in)
+            stream.wait_event(ev_in[sl])
+            if i >= slots:
+                stream.wait_event(ev_out[sl])  # step i-2's results have been copied out
+            ekw = dict(mask=din.get("mask"), colranges=din.get("colranges"), bias=din.get("bias"),
                        causal=wl.causal, scale=wl.scale)
-            fdma.classify_blocks(dev_in["q"], dev_in["k"], dev_in["v"], mask=ekw["mask"], colranges=ekw["colranges"],
-                                 causal=wl.causal, workspace=wsp)
-            fdma.fwd(dev_in["q"], dev_in["k"], dev_in["v"], workspace=wsp, flags=R, out=out, lse=lse, **ekw)
-            fdma.bwd(dev_in["q"], dev_in["k"], dev_in["v"], out, dev_in["dout"], lse, workspace=wsp, flags=R,
-                     grads=grads, **ekw)
-            for h, d in zip(host_out, dev_out):
-                h.copy_(d, non_blocking=True)
+            fdma.classify_blocks(din["q"], din["k"], din["v"], mask=ekw["mask"], colranges=ekw["colranges"],
+                                 causal=wl.causal, workspace=wsp, stream=stream)
+            fdma.fwd(din["q"], din["k"], din["v"], workspace=wsp, flags=R, out=o_, lse=l_, stream=stream, **ekw)
+            fdma.bwd(din["q"], din["k"], din["v"], o_, din["dout"], l_, workspace=wsp, flags=R, grads=g_,
+                     stream=stream, **ekw)
+            ev_done[sl].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[sl])
+                for h, d in zip(hout, [t for t in (o_, l_, *g_) if t is not None]):
+                    h.copy_(d, non_blocking=True)
+                ev_out[sl].record(s_out)
 
-        e2e_step()
+        for i in range(slots):
+            e2e_step(i)
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
         s0 = torch.cuda.Event(enable_timing=True)
         s1 = torch.cuda.Event(enable_timing=True)
         s0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
+        s_in.wait_event(s0)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        for ev in ev_out:
+            stream.wait_event(ev)  # every step's results are on the host
         s1.record(stream)
         torch.cuda.synchronize()
         e2e = s0.elapsed_time(s1) / e2e_steps
+        assert fdma.device_error() == 0
     ms_e2e = e2e if e2e is not None else -1.0
 
     ms_total, ms_e2e, ms_bwd, ms_fwd, ms_cls = max_over_ranks([ms_total, ms_e2e, ms_bwd, ms_fwd, ms_cls], dist, dev)
@@ -336,7 +364,10 @@ def run_gpu(args):
                      "traffic_note": ("ncu dram bytes of one bwd_kernel launch (profiles/)" if traffic is not None
                                       else "null: no ncu capture of the current bwd_kernel on this workload")},
         "e2e": ({"value": round(whole_job_tflops(flops, ws, ms_e2e), 3), "unit": "TFLOP/s",
-                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3)}
+                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3),
+                 "copies": "pinned host buffers; each step's copies in and out, pipelined across steps (two "
+                           "device slots: step i+1's host->device and step i-1's device->host copies overlap "
+                           "step i's compute)"}
                 if e2e is not None else
                 {"value": None, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                  "note": "not measured: pinned host copies of this workload exceed the bench's host budget"}),
