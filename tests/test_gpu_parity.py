@@ -483,22 +483,36 @@ def test_one_head_per_kv_head_with_bias(F):
     run_and_compare(F, inp, True, wl.scale)
 
 
-@pytest.mark.parametrize("variant", ["bias_g2", "colranges_g3"])
+@pytest.mark.parametrize("variant", ["bias_g2", "colranges_g3", "wide256_bias", "wide192_colranges"])
 def test_bounded_wait_unwind(F, variant):
     """FDMA_FLAG_TEST_SHORT_WAIT makes the softmax / compute warps' first wait expire (a
     barrier nothing arrives at, ~100 us limit): forward and backward report
     FDMA_ERR_TIMEOUT through the device error word, unwind without a fault (copies and
     products drained, TMEM freed), and the next normal calls on the same context match the
-    oracle."""
+    oracle.  The wide variants run the wide one-head forward and both launches of the
+    output-split backward."""
     T = F.FDMA_FLAG_TEST_SHORT_WAIT
     if variant == "bias_g2":  # two-head forward, backward with bias and dBias
         wl = W.scaled(W.WORKLOADS["n4096_hq32_hkv8"], Nq=512, Nk=512, Hq=4, Hkv=2, keep_window=200, seed=91)
         inp = W.make_inputs(wl)
         causal, scale = True, wl.scale
-    else:  # single-head forward (odd group), backward without bias
+    elif variant == "colranges_g3":  # single-head forward (odd group), backward without bias
         wl = W.Workload("doc_unwind", 1, 384, 384, 3, 1, 64, True, 0.125, "colranges", 0, False, doc_lo=50,
                         doc_hi=200, seed=92)
         inp = W.make_inputs(wl)
+        causal, scale = True, wl.scale
+    else:  # head dims 256 / 256 with bias and dBias, 192 / 128 with column ranges
+        d, dv = (256, 256) if variant == "wide256_bias" else (192, 128)
+        if variant == "wide256_bias":
+            wl = W.scaled(W.WORKLOADS["n4096_hq32_hkv8"], Nq=392, Nk=392, Hq=2, Hkv=1, d=d, keep_window=120,
+                          seed=93, scale=d ** -0.5)
+        else:
+            wl = W.Workload("doc_unwind_wide", 1, 392, 392, 2, 2, d, True, d ** -0.5, "colranges", 0, False,
+                            doc_lo=50, doc_hi=200, seed=94)
+        inp = W.make_inputs(wl)
+        g = torch.Generator().manual_seed(95)
+        inp["v"] = torch.randn(wl.B, wl.Nk, wl.Hkv, dv, generator=g).bfloat16()
+        inp["dout"] = torch.randn(wl.B, wl.Nq, wl.Hq, dv, generator=g).bfloat16()
         causal, scale = True, wl.scale
     q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "dout"))
     kw = dict(mask=_cuda(inp.get("mask")), colranges=_cuda(inp.get("colranges")), bias=_cuda(inp.get("bias")),
