@@ -165,6 +165,24 @@ int classify_into_workspace(const fdma_args* a, int8_t* user_map, cudaStream_t s
   p.user_map = user_map;
   p.bits_row = reinterpret_cast<uint4*>(ws + w.bits_row);
   p.bits_col = reinterpret_cast<uint4*>(ws + w.bits_col);
+  if (a->mask_kind == FDMA_MASK_DENSE && (a->mask_stride[2] > 0 || a->Nq == 1)) {
+    // bf16 masks stream through TMA; an axis with stride 0 (broadcast) gets extent 1.  A row
+    // stride of 0 (one mask row for every query) or a layout the tensor map refuses takes the
+    // register-load kernel below.
+    const bool bb = a->mask_stride[0] == 0, bh = a->mask_stride[1] == 0;
+    const uint64_t dims[4] = {static_cast<uint64_t>(a->Nk), static_cast<uint64_t>(a->Nq),
+                              bh ? 1ull : static_cast<uint64_t>(a->Hkv), bb ? 1ull : static_cast<uint64_t>(a->B)};
+    const uint64_t sb[3] = {static_cast<uint64_t>(a->mask_stride[2]) * 2, static_cast<uint64_t>(a->mask_stride[1]) * 2,
+                            static_cast<uint64_t>(a->mask_stride[0]) * 2};
+    CUtensorMap tm;
+    p.err = device_error_word();
+    if (p.err == nullptr) return FDMA_ERR_CUDA;
+    if (make_map(&tm, a->mask, dims, sb)) {
+      p.mask_bsel = bb ? 0 : 1;
+      p.mask_hsel = bh ? 0 : 1;
+      return launch_classify_tma1(tm, p, stream) == cudaSuccess ? FDMA_OK : FDMA_ERR_CUDA;
+    }
+  }
   return launch_classify(p, stream) == cudaSuccess ? FDMA_OK : FDMA_ERR_CUDA;
 }
 

@@ -47,6 +47,8 @@ struct ClassifyParams {
   int B, Nq, Nk, Hkv, nTq, nTk;
   int mask_kind, causal, no_skip;
   int causal_off;  // key j is visible from query i when j <= i + causal_off (Nk - Nq, or q_offset)
+  int mask_bsel, mask_hsel;  // bf16 masks by TMA: 0 where the mask is broadcast (coordinate 0)
+  int* err;                  // device error word (the TMA classifier's bounded wait)
   const uint16_t* mask;
   const uint8_t* mask_u8;  // same buffer, FDMA_MASK_DENSE_U8 / FDMA_MASK_BITS
   int64_t ms_b, ms_h, ms_r;
@@ -138,6 +140,8 @@ struct TopkParams {
 };
 
 cudaError_t launch_classify(const ClassifyParams& p, cudaStream_t stream);
+// bf16 masks through a tensor map of the mask (4D, 64 x 128 box, 128-byte swizzle).
+cudaError_t launch_classify_tma1(const CUtensorMap& tm, const ClassifyParams& p, cudaStream_t stream);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
 size_t topk_smem_bytes(int Nk);
 cudaError_t launch_fwd(int d, int dv, bool has_bias, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
