@@ -9,10 +9,11 @@
 // 128 / 128, part 1 64 / 0; 256 / 256: 128 / 128 twice).  Every CTA of a part recomputes
 // S^T = K Q^T and dP^T = V dO^T over the full widths and accumulates only its own columns:
 //   TMEM   S^T / P^T 0..127, dP^T and then dQ 128..255, dV 256.., dK 384..
-//   smem   Q (full width), the part's K columns (resident), a buffer X that holds the other K
-//          columns until S^T has read them and then dO, a two-slot ring that streams V in
-//          64-column chunks, and a buffer that holds a query tile's bias until the compute
-//          warps have copied it into registers and then each step's dS^T.
+//   smem   Q (full width); at 192 / 128 all of K and V resident and X holding dO; at 256 / 256
+//          the part's K columns resident, a buffer X that holds the other K columns until S^T
+//          has read them and then dO, and a two-slot ring that streams V in 64-column chunks;
+//          and a buffer that holds a query tile's bias until the compute warps have copied it
+//          into registers and then each step's dS^T.
 // One CTA = (batch, kv head, 128-key tile) of one part.  Roles: warp 0 TMA producer, warp 1
 // MMA issuer, warps 4..11 two compute warpgroups (keys on TMEM lanes, 64 queries each; P pass,
 // then dS pass), warps 12..15 dQ drain (fp32 reductions into the (B, nqpad, Hq, d) accumulator).
@@ -67,12 +68,19 @@ struct WideSmem {
   static constexpr int kVC = DV / 64;        // V / dO chunks
   static constexpr int kKjC = KW / 64;       // the part's K chunks
   static constexpr int kKoC = kQC - kKjC;    // the other K chunks
-  static constexpr int kXC = kKoC > kVC ? kKoC : kVC;
+  static constexpr uint32_t kTail = 32768u + 1024u + kNumWideBars * 8u + 16u + kMaxKTiles / 4;
+  // Resident plan, where it fits (192 / 128): all of K and all of V stay in shared memory for the
+  // CTA's life and X holds only dO.  Otherwise (256 / 256) the part's K columns stay, X takes the
+  // other K columns and then dO each step, and V streams through a two-slot ring of chunks.
+  static constexpr bool kRes = (2u * kQC + 2u * kVC) * 16384u + kTail <= 232448u;
+  static constexpr int kKC = kRes ? kQC : kKjC;  // K chunks kept (all, or the part's)
+  static constexpr int kXC = kRes ? kVC : (kKoC > kVC ? kKoC : kVC);
+  static constexpr int kVS = kRes ? kVC : 2;     // V chunks kept, or ring slots
   static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffKj = kOffQ + kQC * 16384u;
-  static constexpr uint32_t kOffX = kOffKj + kKjC * 16384u;
-  static constexpr uint32_t kOffV = kOffX + kXC * 16384u;  // 2 slots
-  static constexpr uint32_t kOffBD = kOffV + 2 * 16384u;   // bias tile / dS^T tile (32 KB)
+  static constexpr uint32_t kOffKj = kOffQ + kQC * 16384u;  // K: all chunks (resident) or the part's
+  static constexpr uint32_t kOffX = kOffKj + kKC * 16384u;
+  static constexpr uint32_t kOffV = kOffX + kXC * 16384u;
+  static constexpr uint32_t kOffBD = kOffV + kVS * 16384u;  // bias tile / dS^T tile (32 KB)
   static constexpr uint32_t kOffLse = kOffBD + 32768u;
   static constexpr uint32_t kOffDelta = kOffLse + 512u;
   static constexpr uint32_t kOffBar = kOffDelta + 512u;
@@ -114,6 +122,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   static_assert(VW == 0 || VW == 64 || VW == 128, "part widths are 64 or 128 columns");
   using L = WideSmem<DQK, DV, KW>;
   constexpr int QC = L::kQC, VC = L::kVC, KjC = L::kKjC, KoC = L::kKoC;
+  constexpr bool RES = L::kRes;
   constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);            // S^T, dP^T
   constexpr uint32_t IDESC_DV = idesc_bf16(128, VW > 0 ? VW : 64, false, true);  // P^T(tmem) x dO part
   constexpr uint32_t IDESC_DK = idesc_bf16(128, KW, false, true);             // dS^T x Q part
@@ -184,8 +193,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
       if (HAS_BIAS) tma_prefetch_desc(&tmB);
-      mbar_arrive_expect_tx(&bars[wKjFull], KjC * 16384u);
-      for (int c = 0; c < KjC; ++c) tma_load_4d(sKj + c * 16384, &tmK, &bars[wKjFull], KC0 + c * 64, k0, g, b);
+      if (RES) {  // all of K and V, once
+        mbar_arrive_expect_tx(&bars[wKjFull], (QC + VC) * 16384u);
+        for (int c = 0; c < QC; ++c) tma_load_4d(sKj + c * 16384, &tmK, &bars[wKjFull], c * 64, k0, g, b);
+        for (int c = 0; c < VC; ++c) tma_load_4d(sV + c * 16384, &tmV, &bars[wKjFull], c * 64, k0, g, b);
+      } else {
+        mbar_arrive_expect_tx(&bars[wKjFull], KjC * 16384u);
+        for (int c = 0; c < KjC; ++c) tma_load_4d(sKj + c * 16384, &tmK, &bars[wKjFull], KC0 + c * 64, k0, g, b);
+      }
       int n = 0, nb = 0, nv = 0;      // steps, bias fills, V chunk fills issued
       int nq = 0, nxk = 0, ndo = 0;   // Q, other-K and dO fills issued
       bool ok = true;
@@ -201,8 +216,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           bulk_load(sDelta, p.delta + vec, 512, &bars[wQFull]);
           nq = n + 1;
           // the other K columns, into X once the previous step's dP^T and dV have read dO there
+          // (resident plan: X holds only dO)
           if (!(ok = mbar_wait(&bars[wXFree], (n & 1) ^ 1, p.err, kDevErrTimeout, abort_flag))) break;
-          if (KoC > 0) {
+          if (RES) {
+          } else if (KoC > 0) {
             mbar_arrive_expect_tx(&bars[wXKFull], KoC * 16384u);
             for (int i = 0; i < KoC; ++i) {
               const int c = i < KC0 / 64 ? i : i + KjC;
@@ -223,12 +240,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             ++nb;
           }
           // dO, into X once S^T has read the other K columns
-          if (!(ok = mbar_wait(&bars[wXKFree], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
+          if (!RES && !(ok = mbar_wait(&bars[wXKFree], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
           mbar_arrive_expect_tx(&bars[wDoFull], VC * 16384u);
           for (int c = 0; c < VC; ++c) tma_load_4d(sX + c * 16384, &tmDO, &bars[wDoFull], c * 64, qt * kTile, h, b);
           ndo = n + 1;
-          // V, in 64-column chunks through the two-slot ring
-          for (int c = 0; ok && c < VC; ++c, ++nv) {
+          // V, in 64-column chunks through the two-slot ring (resident plan: loaded once)
+          for (int c = 0; !RES && ok && c < VC; ++c, ++nv) {
             const int s = nv & 1;
             if (!(ok = mbar_wait(&bars[wVEmpty + s], ((nv >> 1) & 1) ^ 1, p.err, kDevErrTimeout, abort_flag))) break;
             mbar_arrive_expect_tx(&bars[wVFull + s], 16384u);
@@ -242,7 +259,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         // of each buffer (of each ring slot) can still be in flight
         mbar_wait(&bars[wKjFull], 0, p.err, kDevErrTimeout, nullptr);
         if (nq > 0) mbar_wait(&bars[wQFull], (nq - 1) & 1, p.err, kDevErrTimeout, nullptr);
-        if (nxk > 0) mbar_wait(&bars[wXKFull], (nxk - 1) & 1, p.err, kDevErrTimeout, nullptr);
+        if (!RES && nxk > 0) mbar_wait(&bars[wXKFull], (nxk - 1) & 1, p.err, kDevErrTimeout, nullptr);
         if (ndo > 0) mbar_wait(&bars[wDoFull], (ndo - 1) & 1, p.err, kDevErrTimeout, nullptr);
         if (nb > 0) mbar_wait(&bars[wBFull], (nb - 1) & 1, p.err, kDevErrTimeout, nullptr);
         for (int m = nv > 2 ? nv - 2 : 0; m < nv; ++m)
@@ -253,7 +270,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       bool ok = mbar_wait(&bars[wKjFull], 0, p.err, kDevErrTimeout, abort_flag);
       const uint64_t dsdesc_k = sdesc_sw128(smem_u32(sBD), 16, 1024);
       const uint64_t dsdesc_mn = sdesc_sw128(smem_u32(sBD), 16384, 1024);
-      const uint64_t kjdesc_mn = sdesc_sw128(smem_u32(sKj), 16384, 1024);
+      const uint64_t kjdesc_mn = sdesc_sw128(smem_u32(sKj + (RES ? (KC0 / 64) * 16384 : 0)), 16384, 1024);
       const uint64_t qdesc_mn = sdesc_sw128(smem_u32(sQ + (KC0 / 64) * 16384), 16384, 1024);
       const uint64_t dodesc_mn = sdesc_sw128(smem_u32(sX + (KC0 / 64) * 16384), 16384, 1024);
       int n = 0, nv = 0;
@@ -262,12 +279,13 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           // S^T = K Q^T over the full q/k width: the part's chunks from their resident copy,
           // the others from X
           if (!(ok = mbar_wait(&bars[wQFull], n & 1, p.err, kDevErrTimeout, abort_flag) &&
-                     mbar_wait(&bars[wXKFull], n & 1, p.err, kDevErrTimeout, abort_flag)))
+                     (RES || mbar_wait(&bars[wXKFull], n & 1, p.err, kDevErrTimeout, abort_flag))))
             break;
           tc_fence_after();
           for (int c = 0; c < QC; ++c) {
             const bool own = c >= KC0 / 64 && c < KC0 / 64 + KjC;
-            const uint8_t* ka = own ? sKj + (c - KC0 / 64) * 16384 : sX + (c < KC0 / 64 ? c : c - KjC) * 16384;
+            const uint8_t* ka = RES ? sKj + c * 16384
+                                    : own ? sKj + (c - KC0 / 64) * 16384 : sX + (c < KC0 / 64 ? c : c - KjC) * 16384;
             const uint64_t adesc = sdesc_sw128(smem_u32(ka), 16, 1024);
             const uint64_t bdesc = sdesc_sw128(smem_u32(sQ + c * 16384), 16, 1024);
             const uint32_t acc0 = c > 0 ? 1u : 0u;
@@ -277,14 +295,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             umma_ss_off<wk_off(3), wk_off(3)>(tbase, adesc, bdesc, IDESC_S, 1u);
           }
           umma_commit(&bars[wSFull]);
-          umma_commit(&bars[wXKFree]);
+          if (!RES) umma_commit(&bars[wXKFree]);
           // dP^T = V dO^T over the full v width into columns 128..255, which the previous
           // step's dQ used
           if (!(ok = mbar_wait(&bars[wDoFull], n & 1, p.err, kDevErrTimeout, abort_flag))) break;
           if (n > 0 && !(ok = mbar_wait(&bars[wDqFree], (n - 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
           for (int c = 0; c < VC; ++c, ++nv) {
-            const int s = nv & 1;
-            if (!(ok = mbar_wait(&bars[wVFull + s], (nv >> 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+            const int s = RES ? c : (nv & 1);  // resident V chunk c, or ring slot
+            if (!RES && !(ok = mbar_wait(&bars[wVFull + s], (nv >> 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
             tc_fence_after();
             const uint64_t adesc = sdesc_sw128(smem_u32(sV + s * 16384), 16, 1024);
             const uint64_t bdesc = sdesc_sw128(smem_u32(sX + c * 16384), 16, 1024);
@@ -293,7 +311,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             umma_ss_off<wk_off(1), wk_off(1)>(tbase + 128, adesc, bdesc, IDESC_S, 1u);
             umma_ss_off<wk_off(2), wk_off(2)>(tbase + 128, adesc, bdesc, IDESC_S, 1u);
             umma_ss_off<wk_off(3), wk_off(3)>(tbase + 128, adesc, bdesc, IDESC_S, 1u);
-            umma_commit(&bars[wVEmpty + s]);
+            if (!RES) umma_commit(&bars[wVEmpty + s]);
           }
           if (!ok) break;
           umma_commit(&bars[wDpFull]);
