@@ -6,6 +6,8 @@ without dBias.  Tolerances as in test_gpu_parity.py, except that O's absolute bo
 relative term: O comes back in bf16 (half an ulp is up to 2^-8 of |O|) and is normalised by
 bf16-rounded weights, so a row with few kept keys and |O| near 4 is off by ~0.014 (measured:
 seed 1039, 13 kept keys, O = 4.2047, returned 4.21875, the nearest bf16)."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -90,7 +92,13 @@ def _case(seed, wide=False):
                 want_dbias=want_dbias)
 
 
-@pytest.mark.parametrize("seed", list(range(1000, 1040)) + [("wide", s) for s in range(2000, 2012)])
+# FDMA_FUZZ_EXTRA=n adds n more seeds from 2100 on, and n/3 more of the wide head dims from 3000
+_EXTRA = int(os.environ.get("FDMA_FUZZ_EXTRA", "0"))
+_SEEDS = (list(range(1000, 1040)) + [("wide", s) for s in range(2000, 2012)] + list(range(2100, 2100 + _EXTRA)) +
+          [("wide", s) for s in range(3000, 3000 + _EXTRA // 3)])
+
+
+@pytest.mark.parametrize("seed", _SEEDS)
 def test_random_problem_matches_oracle(F, seed):
     """Seeds 1000-1039: head dims 8..128; ("wide", 2000-2011): the head-dim pairs 192 / 128 and
     256 / 256, with the other parameters drawn the same way."""
