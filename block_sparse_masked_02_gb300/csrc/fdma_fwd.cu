@@ -13,10 +13,12 @@
 //   warp 1      TMEM owner and single-thread tcgen05.mma issuer:
 //               S_n = Q K_n^T (SS, fp32 in TMEM, double-buffered), then
 //               O += P_{n-1} V_{n-1} with P read from TMEM (TS);
-//   warps 2..5  softmax, one thread per query row (TMEM lane): scale, bias,
-//               mask bits on partial tiles, online max/sum with lazy O
-//               rescaling, P written back to TMEM as packed bf16; final
-//               O / l and lse.
+//   warps 2..5  softmax, one thread per query row (TMEM lane): while S is
+//               computed, the tile's additive term (bias, -inf at masked keys)
+//               is formed from the bias tile and the keep bits; then S is
+//               added with paired fp32 FMAs, a three-input row maximum, lazy O
+//               rescaling, exp2 and P written back to TMEM as packed bf16 with
+//               the row sum of the rounded weights; final O / l and lse.
 // TMEM columns: S[0] 0..127, S[1] 128..255, O 256..256+dv.
 // Head dims: q/k width DQK and v/out width DV are 64 or 128 (equal), or 192 / 128
 // and 256 / 256 (FlashMask README, "Performance", SM100 head-dim table).
@@ -253,60 +255,98 @@ __global__ void __launch_bounds__(192, 1)
     bool ok = !p.test_short_wait ||
               mbar_wait(&bars[kFNever], 0, p.err, kDevErrTimeout, abort_flag, kTestWaitNs);
     uint32_t raw[32];
+    // Row maximum m_ref in the units of u: u = S*scale + bias with a bias, u = S without one
+    // (scale > 0); the softmax exponent in log2 units is u*cexp - m_ref*cexp.
+    const float cexp = HAS_BIAS ? kLog2e : p.scale_log2;
+    const float thr_u = kRescaleThreshold / cexp;
+    const uint64_t c2 = f2(cexp, cexp);
+    const uint64_t sc2 = f2(p.scale, p.scale);
+    // The keep bits of a partial tile are fetched one active tile ahead, so their load latency
+    // overlaps the wait for S.
+    auto is_partial = [&](int kt) { return map_row[kt] == kPartial || (ragged_k && kt == p.nTk - 1); };
+    uint4 bits_next = make_uint4(~0u, ~0u, ~0u, ~0u);
+    if (first_kt < p.nTk && is_partial(first_kt)) bits_next = __ldg(&p.bits_row[(tile_base + first_kt) * kTile + r]);
     for (int kt = first_kt; ok && kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
       const int s = n & 1;
       const uint32_t ph = (n >> 1) & 1;
-      if (!(ok = mbar_wait(&bars[kSFull + s], ph, p.err, kDevErrTimeout, abort_flag))) break;
-      tc_fence_after();
-      const bool partial = map_row[kt] == kPartial || (ragged_k && kt == p.nTk - 1);
-      uint4 bits = make_uint4(~0u, ~0u, ~0u, ~0u);
-      if (partial) bits = __ldg(&p.bits_row[(tile_base + kt) * kTile + r]);
-      float x[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(tl + s * 128 + c * 32, raw);
-        tmem_ld_wait(raw);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[c * 32 + j] = __uint_as_float(raw[j]) * p.scale_log2;
+      const bool partial = is_partial(kt);
+      const uint4 bits = bits_next;
+      {
+        const int kn = next_active(map_row, kt, p.nTk);
+        bits_next = make_uint4(~0u, ~0u, ~0u, ~0u);
+        if (kn < p.nTk && is_partial(kn)) bits_next = __ldg(&p.bits_row[(tile_base + kn) * kTile + r]);
       }
+      // Additive term of this tile, formed while S is still being computed: the bias
+      // (u = S*scale + bias) and/or -inf at the masked keys (u = S + 0 / -inf).
+      const bool addend = HAS_BIAS || partial;
+      uint64_t u[64];  // u of keys 2t, 2t+1
       if (HAS_BIAS) {
         const int sb = n % BS;
         if (!(ok = mbar_wait(&bars[kBFull + sb], (n / BS) & 1, p.err, kDevErrTimeout, abort_flag))) break;
         const uint8_t* bt = sB + sb * L::kBB + r * 128;
 #pragma unroll
         for (int cc = 0; cc < 16; ++cc) {
-          const uint4 v = *reinterpret_cast<const uint4*>(bt + (cc >> 3) * 16384 + (((cc & 7) ^ (r & 7)) << 4));
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          const uint4 bv = *reinterpret_cast<const uint4*>(bt + (cc >> 3) * 16384 + (((cc & 7) ^ (r & 7)) << 4));
+          const uint32_t wv[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            x[cc * 8 + 2 * e] = fmaf(__uint_as_float(w[e] << 16), kLog2e, x[cc * 8 + 2 * e]);
-            x[cc * 8 + 2 * e + 1] = fmaf(__uint_as_float(w[e] & 0xFFFF0000u), kLog2e, x[cc * 8 + 2 * e + 1]);
-          }
+          for (int e = 0; e < 4; ++e) u[cc * 4 + e] = bf16x2_to_f2(wv[e]);
         }
         fence_proxy_async_smem();  // generic reads of the slot before its next TMA write
         mbar_arrive(&bars[kBEmpty + sb]);
+      } else if (partial) {
+#pragma unroll
+        for (int t = 0; t < 64; ++t) u[t] = 0ull;
       }
       if (partial) {
         const uint32_t bw[4] = {bits.x, bits.y, bits.z, bits.w};
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (!((bw[c >> 5] >> (c & 31)) & 1u)) x[c] = kNegInf;
+        for (int t = 0; t < 64; ++t) {
+          float u0, u1;
+          f2split(u[t], u0, u1);
+          if (!((bw[t >> 4] >> ((2 * t) & 31)) & 1u)) u0 = kNegInf;
+          if (!((bw[t >> 4] >> ((2 * t + 1) & 31)) & 1u)) u1 = kNegInf;
+          u[t] = f2(u0, u1);
+        }
+      }
+      if (!(ok = mbar_wait(&bars[kSFull + s], ph, p.err, kDevErrTimeout, abort_flag))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(tl + s * 128 + c * 32, raw);
+        tmem_ld_wait(raw);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const uint64_t s2 = f2(__uint_as_float(raw[2 * t]), __uint_as_float(raw[2 * t + 1]));
+          const int q = c * 16 + t;
+          u[q] = HAS_BIAS ? fma2(s2, sc2, u[q]) : (addend ? add2(s2, u[q]) : s2);
+        }
       }
       float mx8[8];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) mx8[t] = x[t];
+      for (int t = 0; t < 4; ++t) f2split(u[t], mx8[2 * t], mx8[2 * t + 1]);
 #pragma unroll
-      for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int t = 4; t < 64; t += 4) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float a0, a1;
+          f2split(u[t + q], a0, a1);
+          // three-input maximum: the running value and both halves of the pair
+          asm("max.f32 %0, %0, %1, %2;" : "+f"(mx8[2 * q]) : "f"(a0), "f"(a1));
+        }
+      }
+      float mx;
+      asm("max.f32 %0, %1, %2, %3;" : "=f"(mx) : "f"(mx8[0]), "f"(mx8[2]), "f"(mx8[4]));
+      asm("max.f32 %0, %0, %1, %2;" : "+f"(mx) : "f"(mx8[6]), "f"(mx8[1]));
+      asm("max.f32 %0, %0, %1, %2;" : "+f"(mx) : "f"(mx8[3]), "f"(mx8[5]));
+      mx = fmaxf(mx, mx8[7]);
       const float m_new = fmaxf(m_ref, mx);
       float alpha = 1.f;
       bool resc = false;
-      if (m_new > m_ref + kRescaleThreshold) {
+      if (m_new > m_ref + thr_u) {
         if (m_ref == kNegInf) {
           m_ref = m_new;
         } else {
-          alpha = ex2(m_ref - m_new);
+          alpha = ex2((m_ref - m_new) * cexp);
           l *= alpha;
           m_ref = m_new;
           resc = true;
@@ -331,15 +371,17 @@ __global__ void __launch_bounds__(192, 1)
         }
         tmem_st_wait();
       }
-      const float mu = (m_ref == kNegInf) ? 0.f : m_ref;
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      const float nm = (m_ref == kNegInf) ? 0.f : -(m_ref * cexp);
+      const uint64_t nm2 = f2(nm, nm);
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};  // (even pairs, odd pairs) x (low, high) halves
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const float p0 = ex2(x[c * 32 + 2 * j] - mu);
-          const float p1 = ex2(x[c * 32 + 2 * j + 1] - mu);
+          float e0, e1;
+          f2split(fma2(u[c * 16 + j], c2, nm2), e0, e1);
+          const float p0 = ex2(e0), p1 = ex2(e1);
           pk[j] = pack_bf16x2(p0, p1);
           // normalise with the same bf16-rounded weights the PV product uses
           sum4[2 * (j & 1)] = add_bf16lo(pk[j], sum4[2 * (j & 1)]);
@@ -347,7 +389,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         tmem_st16(tl + s * 128 + c * 16, pk);
       }
-      l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      l += (sum4[0] + sum4[2]) + (sum4[1] + sum4[3]);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars[kPReady + s]);
@@ -379,7 +421,7 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       if (i < p.Nq)
-        p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + i] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : kNegInf;
+        p.lse[(static_cast<int64_t>(b) * p.Hq + h) * p.Nq + i] = l > 0.f ? (m_ref * cexp + log2f(l)) * kLn2 : kNegInf;
     }
   }
   tc_fence_before();
