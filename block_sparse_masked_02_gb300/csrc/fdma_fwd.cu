@@ -20,8 +20,9 @@
 //               rescaling, exp2 and P written back to TMEM as packed bf16 with
 //               the row sum of the rounded weights; final O / l and lse.
 // TMEM columns: S[0] 0..127, S[1] 128..255, O 256..256+dv.
-// Head dims: q/k width DQK and v/out width DV are 64 or 128 (equal), or 192 / 128
-// and 256 / 256 (FlashMask README, "Performance", SM100 head-dim table).
+// This one-head kernel serves the wide head dims, q/k width DQK and v/out width DV
+// of 192 / 128 and 256 / 256 (FlashMask README, "Performance", SM100 head-dim
+// table); head dims up to 128 run on the two-slot kernel further down.
 #include "fdma_internal.h"
 #include "fdma_ptx.cuh"
 
@@ -434,9 +435,13 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ============================================================================
-// Two-head forward (used when the GQA group size is even).  One CTA = one
-// (batch, kv head, 128-row query tile, pair of query heads of the group):
+// Two-slot forward (head dims up to 128).  Even GQA group sizes: one CTA = one
+// (batch, kv head, 128-row query tile, pair of query heads of the group), and
 // both heads read the same K, V, bias and mask tiles, which are fetched once.
+// Odd group sizes and MHA (QP): one CTA = one (batch, query head, pair of
+// adjacent query tiles 2t, 2t+1); the two tiles share K and V, each has its
+// own bias rows and block-map row, and a key tile only one of them needs is
+// skipped by the other (the MMA issuer walks the union of the two rows).
 // Warps: warpgroup 0 = {TMA producer, MMA issuer, 2 idle}, warpgroup 1 =
 // softmax of head 0, warpgroup 2 = softmax of head 1 (setmaxnreg moves
 // registers to the softmax groups).  While a softmax warp waits for S it turns
@@ -481,7 +486,11 @@ struct Fwd2Smem {
   static constexpr uint32_t kTotal = kOffMisc + 16;
 };
 
-template <int D, bool HAS_BIAS>
+// QP (odd group sizes, MHA): the two slots are one head's query tiles 2t and 2t+1 instead of two
+// heads of one query tile.  Both slots walk the union of their active key tiles (K and V are the
+// same); a tile one slot does not need is fully masked for it (P = 0); each slot has its own
+// bias buffer (its own rows), one deep.
+template <int D, bool HAS_BIAS, bool QP>
 __global__ void __launch_bounds__(kFwd2Threads, 1)
     fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmB,
@@ -498,19 +507,36 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int GP = p.G >> 1;  // head pairs per group
   int id = blockIdx.x;
-  const int hp = id % GP;
-  id /= GP;
-  const int g = id % p.Hkv;
-  id /= p.Hkv;
-  const int b = id % p.B;
-  id /= p.B;
-  const int qt = p.nTq - 1 - id;  // longest causal rows first
-  const int h0 = g * p.G + 2 * hp;
+  int g, b, h0, qt;
+  if (QP) {  // (query-tile pair, head): slot w is query tile 2 * pair + w of head h0
+    const int hq = id % p.Hq;
+    id /= p.Hq;
+    b = id % p.B;
+    id /= p.B;
+    qt = 2 * (((p.nTq + 1) >> 1) - 1 - id);  // longest causal rows first
+    h0 = hq;
+    g = hq / p.G;
+  } else {  // (query tile, head pair of one group)
+    const int GP = p.G >> 1;
+    const int hp = id % GP;
+    id /= GP;
+    g = id % p.Hkv;
+    id /= p.Hkv;
+    b = id % p.B;
+    id /= p.B;
+    qt = p.nTq - 1 - id;  // longest causal rows first
+    h0 = g * p.G + 2 * hp;
+  }
   const int q0 = qt * kTile;
   const int64_t tile_base = (static_cast<int64_t>(b * p.Hkv + g) * p.nTq + qt) * p.nTk;
   const bool ragged_k = (p.Nk & (kTile - 1)) != 0;
+  // slot w's query tile (QP: qt + w, possibly past the last tile), head and class of key tile kt
+  auto slot_q0 = [&](int w) { return QP ? q0 + w * kTile : q0; };
+  auto slot_head = [&](int w) { return QP ? h0 : h0 + w; };
+  auto slot_cls = [&](int w, int kt) {
+    return QP ? ((map_row[kt] >> (2 * w)) & 3) : static_cast<int>(map_row[kt]);
+  };
 
   if ((smem_u32(smem) & 1023u) != 0) {
     if (threadIdx.x == 0) atomicCAS(p.err, 0, kDevErrAlign);
@@ -518,13 +544,21 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumFwd2Bars; ++i) mbar_init(&bars[i], 1);
-    mbar_init(&bars[k2BEmpty + 0], 256);
-    mbar_init(&bars[k2BEmpty + 1], 256);
+    mbar_init(&bars[k2BEmpty + 0], QP ? 128 : 256);  // QP: each bias buffer serves one slot
+    mbar_init(&bars[k2BEmpty + 1], QP ? 128 : 256);
     for (int i = 0; i < 4; ++i) mbar_init(&bars[k2PReady + i], 128);
     misc[1] = 0;
     fence_mbar_init();
   }
-  for (int kt = threadIdx.x; kt < p.nTk; kt += blockDim.x) map_row[kt] = p.kmap[tile_base + kt];
+  for (int kt = threadIdx.x; kt < p.nTk; kt += blockDim.x) {
+    if (QP) {  // both slots' classes: bits 0-1 slot 0, bits 2-3 slot 1 (zero iff both skip)
+      const int c0 = p.kmap[tile_base + kt];
+      const int c1 = qt + 1 < p.nTq ? p.kmap[tile_base + p.nTk + kt] : kSkip;
+      map_row[kt] = static_cast<int8_t>(c0 | (c1 << 2));
+    } else {
+      map_row[kt] = p.kmap[tile_base + kt];
+    }
+  }
   if (warp == 1) {
     tmem_alloc(misc, 512);
     tmem_relinquish();
@@ -554,8 +588,9 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
       for (int w = 0; w < 2; ++w)
 #pragma unroll
         for (int c = 0; c < KB; ++c)
-          tma_load_4d(sQ + w * L::kQB + c * 16384, &tmQ, &bars[k2QFull], c * 64, q0, h0 + w, b);
+          tma_load_4d(sQ + w * L::kQB + c * 16384, &tmQ, &bars[k2QFull], c * 64, slot_q0(w), slot_head(w), b);
       int n = 0, items = 0, nbias = 0;
+      int nbw[2] = {0, 0};  // QP: bias fills per slot
       bool ok = true;
       for (int kt = first_kt; ok && kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
         const int k0 = kt * kTile;
@@ -569,7 +604,20 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
             tma_load_4d(sKV + sl * L::kQB + c * 16384, &tmK, &bars[k2KvFull + sl], c * 64, k0, g, b);
           items = it + 1;
         }
-        if (HAS_BIAS) {
+        if (HAS_BIAS && QP) {
+          // each slot's own bias rows, into its own buffer (one deep), for the tiles it needs
+          for (int w = 0; ok && w < 2; ++w) {
+            if (slot_cls(w, kt) == kSkip) continue;
+            if (!(ok = mbar_wait(&bars[k2BEmpty + w], (nbw[w] & 1) ^ 1, p.err, kDevErrTimeout, abort_flag))) break;
+            mbar_arrive_expect_tx(&bars[k2BFull + w], L::kBB);
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+              tma_load_4d_hint(sB + w * L::kBB + c * 16384, &tmB, &bars[k2BFull + w], k0 + c * 64, slot_q0(w),
+                               g * p.bias_hsel, b * p.bias_bsel, bias_pol);
+            ++nbw[w];
+          }
+          if (!ok) break;
+        } else if (HAS_BIAS) {
           const int sb = n & 1;
           if (!(ok = mbar_wait(&bars[k2BEmpty + sb], ((n >> 1) & 1) ^ 1, p.err, kDevErrTimeout, abort_flag))) break;
           mbar_arrive_expect_tx(&bars[k2BFull + sb], L::kBB);
@@ -595,8 +643,13 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
         for (int it = items > 3 ? items - 3 : 0; it < items; ++it)
           mbar_wait(&bars[k2KvFull + it % 3], (it / 3) & 1, p.err, kDevErrTimeout, nullptr);
         // and the last fill of each bias slot
-        for (int m = nbias > 2 ? nbias - 2 : 0; m < nbias; ++m)
-          mbar_wait(&bars[k2BFull + (m & 1)], (m >> 1) & 1, p.err, kDevErrTimeout, nullptr);
+        if (QP) {
+          for (int w = 0; w < 2; ++w)
+            if (nbw[w] > 0) mbar_wait(&bars[k2BFull + w], (nbw[w] - 1) & 1, p.err, kDevErrTimeout, nullptr);
+        } else {
+          for (int m = nbias > 2 ? nbias - 2 : 0; m < nbias; ++m)
+            mbar_wait(&bars[k2BFull + (m & 1)], (m >> 1) & 1, p.err, kDevErrTimeout, nullptr);
+        }
       }
     } else if (warp == 1 && lane == 0 && any_active) {
       // ---------------------------------------------------------------- MMA issuer
@@ -618,22 +671,57 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
       };
       // O_w += P_w V, in two key halves, each issued once its P is stored; P of keys
       // 16k .. 16k+15 sits in S_w's columns 8k .. 8k+7
-      auto pv_when_ready = [&](int w, int m) {
+      // (V of union tile m; j = the slot's own P count: its phase and whether O starts here)
+      auto pv_when_ready = [&](int w, int m, int j) {
         const int sl = (2 * m + 1) % 3;
         const uint64_t vd = kvmn0 + sl * slot_step;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          if (!mbar_wait(&bars[k2PReady + 2 * w + hf], m & 1, p.err, kDevErrTimeout, abort_flag)) return false;
+          if (!mbar_wait(&bars[k2PReady + 2 * w + hf], j & 1, p.err, kDevErrTimeout, abort_flag)) return false;
           tc_fence_after();
 #pragma unroll
           for (int k = hf * 4; k < hf * 4 + 4; ++k)
             umma_ts(tbase + 256 + w * 128, tbase + w * 128 + k * 8, vd + static_cast<uint64_t>((k * 2048) >> 4),
-                    IDESC_O, (m > 0 || k > 0) ? 1u : 0u);
+                    IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
         }
         return true;
       };
       int n = 0;
-      for (int kt = first_kt; ok && kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
+      if constexpr (QP) {
+        // Per union tile n: each slot's pending PV (its tile n-1, if it had one) and then, if the
+        // slot needs tile n, its S(n).  PV_w always precedes S_w of the slot's next tile.
+        int sw[2] = {0, 0};      // S products issued per slot
+        bool pend[2] = {false, false};
+        for (int kt = first_kt; ok && kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
+          const int itk = 2 * n;
+          for (int w = 0; ok && w < 2; ++w) {
+            if (pend[w]) {
+              const int itv = 2 * (n - 1) + 1;
+              if (!(ok = mbar_wait(&bars[k2KvFull + itv % 3], (itv / 3) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+              if (!(ok = pv_when_ready(w, n - 1, sw[w] - 1))) break;
+              pend[w] = false;
+            }
+            if (slot_cls(w, kt) != kSkip) {
+              if (!(ok = mbar_wait(&bars[k2KvFull + itk % 3], (itk / 3) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+              tc_fence_after();
+              issue_s(w, n);
+              ++sw[w];
+              pend[w] = true;
+            }
+          }
+          if (!ok) break;
+          if (n > 0) umma_commit(&bars[k2KvEmpty + (2 * (n - 1) + 1) % 3]);  // V_{n-1}: both slots' PV issued
+          umma_commit(&bars[k2KvEmpty + itk % 3]);                            // K_n: read by this tile's S
+        }
+        if (ok && n > 0) {
+          const int itv = 2 * (n - 1) + 1;
+          ok = mbar_wait(&bars[k2KvFull + itv % 3], (itv / 3) & 1, p.err, kDevErrTimeout, abort_flag);
+          for (int w = 0; ok && w < 2; ++w)
+            if (pend[w]) ok = pv_when_ready(w, n - 1, sw[w] - 1);
+          if (ok) umma_commit(&bars[k2KvEmpty + itv % 3]);
+        }
+      }
+      for (int kt = first_kt; !QP && ok && kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
         const int itk = 2 * n;
         if (n == 0) {
           if (!(ok = mbar_wait(&bars[k2KvFull + itk % 3], (itk / 3) & 1, p.err, kDevErrTimeout, abort_flag))) break;
@@ -647,19 +735,19 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
         // ring slot frees only when the tile before that is done)
         const int m = n - 1, itv = 2 * m + 1;
         if (!(ok = mbar_wait(&bars[k2KvFull + itv % 3], (itv / 3) & 1, p.err, kDevErrTimeout, abort_flag))) break;
-        if (!(ok = pv_when_ready(0, m))) break;
+        if (!(ok = pv_when_ready(0, m, m))) break;
         if (!(ok = mbar_wait(&bars[k2KvFull + itk % 3], (itk / 3) & 1, p.err, kDevErrTimeout, abort_flag))) break;
         tc_fence_after();
         issue_s(0, n);
-        if (!(ok = pv_when_ready(1, m))) break;
+        if (!(ok = pv_when_ready(1, m, m))) break;
         umma_commit(&bars[k2KvEmpty + itv % 3]);
         issue_s(1, n);
         umma_commit(&bars[k2KvEmpty + itk % 3]);
       }
-      if (ok && n > 0) {
+      if (!QP && ok && n > 0) {
         const int m = n - 1, itv = 2 * m + 1;
         ok = mbar_wait(&bars[k2KvFull + itv % 3], (itv / 3) & 1, p.err, kDevErrTimeout, abort_flag) &&
-             pv_when_ready(0, m) && pv_when_ready(1, m);
+             pv_when_ready(0, m, m) && pv_when_ready(1, m, m);
         if (ok) umma_commit(&bars[k2KvEmpty + itv % 3]);
       }
       umma_commit(&bars[k2OFinal]);
@@ -669,11 +757,12 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
   } else {
     regs_increase<kFwd2RegsHigh>();
     // ------------------------------------------------------------------ softmax
-    const int w = (warp >> 2) - 1;  // head within the pair
-    const int h = h0 + w;
+    const int w = (warp >> 2) - 1;  // slot: head within the pair (QP: query tile within the pair)
+    const int h = slot_head(w);
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
-    const int i = q0 + r;
+    const int i = slot_q0(w) + r;
+    const int64_t my_base = tile_base + (QP ? w * p.nTk : 0);  // this slot's row of the block map
     const uint32_t tl = tbase + (static_cast<uint32_t>(quad * 32) << 16);
     const uint32_t scol = w * 128, ocol = 256 + w * 128;
     // Row maximum m_ref is kept in the units of u: u = S*scale + bias with a bias, u = S
@@ -690,24 +779,53 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
     uint32_t raw[32];
     // The keep bits of a partial tile are fetched one active tile ahead, so their
     // load latency overlaps the wait for S.
-    auto is_partial = [&](int kt) { return map_row[kt] == kPartial || (ragged_k && kt == p.nTk - 1); };
+    auto is_partial = [&](int kt) {
+      if constexpr (QP) {
+        const int c = slot_cls(w, kt);
+        return c == kPartial || (c == kFull && ragged_k && kt == p.nTk - 1);
+      } else {
+        return map_row[kt] == kPartial || (ragged_k && kt == p.nTk - 1);
+      }
+    };
+    // this slot's active key tiles (QP: its own row of the block map; otherwise the shared row)
+    auto next_mine = [&](int kt) {
+      if constexpr (QP) {
+        do {
+          ++kt;
+        } while (kt < p.nTk && slot_cls(w, kt) == kSkip);
+        return kt;
+      } else {
+        return next_active(map_row, kt, p.nTk);
+      }
+    };
+    const int first_mine = QP ? next_mine(-1) : first_kt;
     uint4 bits_next = make_uint4(~0u, ~0u, ~0u, ~0u);
-    if (first_kt < p.nTk && is_partial(first_kt)) bits_next = __ldg(&p.bits_row[(tile_base + first_kt) * kTile + r]);
-    for (int kt = first_kt; ok && kt < p.nTk; kt = next_active(map_row, kt, p.nTk), ++n) {
+    if (first_mine < p.nTk && is_partial(first_mine)) bits_next = __ldg(&p.bits_row[(my_base + first_mine) * kTile + r]);
+    for (int kt = first_mine; ok && kt < p.nTk; kt = next_mine(kt), ++n) {
       const bool partial = is_partial(kt);
       const uint4 bits = bits_next;
       {
-        const int kn = next_active(map_row, kt, p.nTk);
+        const int kn = next_mine(kt);
         bits_next = make_uint4(~0u, ~0u, ~0u, ~0u);
-        if (kn < p.nTk && is_partial(kn)) bits_next = __ldg(&p.bits_row[(tile_base + kn) * kTile + r]);
+        if (kn < p.nTk && is_partial(kn)) bits_next = __ldg(&p.bits_row[(my_base + kn) * kTile + r]);
       }
       // Additive term of this tile, formed while S is still being computed: the bias
       // (u = S*scale + bias) and/or -inf at the masked keys (u = S + 0 / -inf).
+      // (no bias, QP: the keep bits select on S as it is read, so no u is held across the wait)
+      constexpr bool kPreMask = HAS_BIAS || !QP;
       const bool addend = HAS_BIAS || partial;
       uint64_t u[64];  // u of keys 2t, 2t+1
       if (HAS_BIAS) {
-        const int sb = n & 1;
-        if (!(ok = mbar_wait(&bars[k2BFull + sb], (n >> 1) & 1, p.err, kDevErrTimeout, abort_flag))) break;
+        int sb;
+        uint32_t bph;
+        if constexpr (QP) {  // one fill per own tile, one deep
+          sb = w;
+          bph = n & 1;
+        } else {
+          sb = n & 1;
+          bph = (n >> 1) & 1;
+        }
+        if (!(ok = mbar_wait(&bars[k2BFull + sb], bph, p.err, kDevErrTimeout, abort_flag))) break;
         const uint8_t* bt = sB + sb * L::kBB + r * 128;
 #pragma unroll
         for (int cc = 0; cc < 16; ++cc) {
@@ -718,11 +836,11 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
         }
         fence_proxy_async_smem();  // generic reads of the slot before its next TMA write
         mbar_arrive(&bars[k2BEmpty + sb]);
-      } else if (partial) {
+      } else if (kPreMask && partial) {
 #pragma unroll
         for (int t = 0; t < 64; ++t) u[t] = 0ull;
       }
-      if (partial) {
+      if (kPreMask && partial) {
         const uint32_t bw[4] = {bits.x, bits.y, bits.z, bits.w};
 #pragma unroll
         for (int t = 0; t < 64; ++t) {
@@ -741,9 +859,19 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
         tmem_ld_wait(raw);
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
-          const uint64_t s2 = f2(__uint_as_float(raw[2 * t]), __uint_as_float(raw[2 * t + 1]));
           const int q = c * 16 + t;
-          u[q] = HAS_BIAS ? fma2(s2, sc2, u[q]) : (addend ? add2(s2, u[q]) : s2);
+          if constexpr (kPreMask) {
+            const uint64_t s2 = f2(__uint_as_float(raw[2 * t]), __uint_as_float(raw[2 * t + 1]));
+            u[q] = HAS_BIAS ? fma2(s2, sc2, u[q]) : (addend ? add2(s2, u[q]) : s2);
+          } else {
+            float s0 = __uint_as_float(raw[2 * t]), s1 = __uint_as_float(raw[2 * t + 1]);
+            if (partial) {
+              const uint32_t bw = (q >> 4) == 0 ? bits.x : (q >> 4) == 1 ? bits.y : (q >> 4) == 2 ? bits.z : bits.w;
+              if (!((bw >> ((2 * q) & 31)) & 1u)) s0 = kNegInf;
+              if (!((bw >> ((2 * q + 1) & 31)) & 1u)) s1 = kNegInf;
+            }
+            u[q] = f2(s0, s1);
+          }
         }
       }
       float mx8[8];
@@ -856,18 +984,19 @@ __global__ void __launch_bounds__(kFwd2Threads, 1)
   }
 }
 
-template <int D, bool HB>
+template <int D, bool HB, bool QP>
 cudaError_t launch_fwd2_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tb,
                           const FwdParams& p, cudaStream_t stream) {
   using L = Fwd2Smem<D, HB>;
-  auto kern = fwd2_kernel<D, HB>;
+  auto kern = fwd2_kernel<D, HB, QP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes fa;
   e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < kFwd2MinLaunchRegs) return cudaErrorInvalidConfiguration;  // setmaxnreg split must fit
-  const unsigned grid = static_cast<unsigned>(p.B) * p.Hkv * (p.G / 2) * p.nTq;
+  const unsigned grid = QP ? static_cast<unsigned>(p.B) * p.Hq * ((p.nTq + 1) / 2)
+                           : static_cast<unsigned>(p.B) * p.Hkv * (p.G / 2) * p.nTq;
   kern<<<grid, kFwd2Threads, L::kTotal, stream>>>(tq, tk, tv, tb, p);
   return cudaGetLastError();
 }
@@ -895,16 +1024,17 @@ cudaError_t launch_fwd(int d, int dv, bool has_bias, const CUtensorMap& tq, cons
     return has_bias ? launch_fwd_t<256, 256, true>(tq, tk, tv, tb, p, stream)
                     : launch_fwd_t<256, 256, false>(tq, tk, tv, tb, p, stream);
   if (dv != d) return cudaErrorInvalidValue;
+  // even groups: two heads of a group per CTA; odd groups: two query tiles of a head per CTA
   if (p.G % 2 == 0) {
-    if (d == 128) return has_bias ? launch_fwd2_t<128, true>(tq, tk, tv, tb, p, stream)
-                                  : launch_fwd2_t<128, false>(tq, tk, tv, tb, p, stream);
-    if (d == 64) return has_bias ? launch_fwd2_t<64, true>(tq, tk, tv, tb, p, stream)
-                                 : launch_fwd2_t<64, false>(tq, tk, tv, tb, p, stream);
+    if (d == 128) return has_bias ? launch_fwd2_t<128, true, false>(tq, tk, tv, tb, p, stream)
+                                  : launch_fwd2_t<128, false, false>(tq, tk, tv, tb, p, stream);
+    if (d == 64) return has_bias ? launch_fwd2_t<64, true, false>(tq, tk, tv, tb, p, stream)
+                                 : launch_fwd2_t<64, false, false>(tq, tk, tv, tb, p, stream);
   }
-  if (d == 128) return has_bias ? launch_fwd_t<128, 128, true>(tq, tk, tv, tb, p, stream)
-                                : launch_fwd_t<128, 128, false>(tq, tk, tv, tb, p, stream);
-  if (d == 64) return has_bias ? launch_fwd_t<64, 64, true>(tq, tk, tv, tb, p, stream)
-                               : launch_fwd_t<64, 64, false>(tq, tk, tv, tb, p, stream);
+  if (d == 128) return has_bias ? launch_fwd2_t<128, true, true>(tq, tk, tv, tb, p, stream)
+                                : launch_fwd2_t<128, false, true>(tq, tk, tv, tb, p, stream);
+  if (d == 64) return has_bias ? launch_fwd2_t<64, true, true>(tq, tk, tv, tb, p, stream)
+                               : launch_fwd2_t<64, false, true>(tq, tk, tv, tb, p, stream);
   return cudaErrorInvalidValue;
 }
 

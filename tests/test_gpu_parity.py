@@ -433,7 +433,8 @@ def test_other_head_dims(F, d, Hq, Hkv):
 def test_small_head_dims(F, d, Hq, Hkv, kind):
     """Head dims below 64 (multiples of 8) run on the 64-wide kernels with the missing columns
     of Q, K, V and dO read as zeros: outputs and all four gradients match the oracle, for the
-    two-head and the one-head forward (even and odd group sizes)."""
+    two-slot forward in both its modes (two heads of an even group; two query tiles of one head
+    for odd groups)."""
     if kind == "bias":
         wl = W.scaled(W.WORKLOADS["n4096_hq32_hkv8"], Nq=392, Nk=392, Hq=Hq, Hkv=Hkv, d=d, keep_window=110,
                       seed=70 + d + Hq, scale=1.0 / math.sqrt(d))
@@ -475,6 +476,30 @@ def test_wide_head_dims(F, d, dv, Hq, Hkv, kind, causal):
     run_and_compare(F, inp, causal, scale, case=f"d{d}/dv{dv} hq{Hq} hkv{Hkv} {kind}")
 
 
+@pytest.mark.parametrize("d,Hq,Hkv,Nq,Nk,with_bias,causal", [
+    (128, 3, 1, 300, 392, True, False), (128, 2, 2, 520, 392, False, False), (64, 1, 1, 300, 296, True, True),
+    (64, 3, 1, 424, 296, False, True), (128, 5, 5, 172, 264, True, False)])
+def test_paired_query_tiles(F, d, Hq, Hkv, Nq, Nk, with_bias, causal):
+    """Odd group sizes and MHA run the two-slot forward with one head's query tiles 2t and 2t+1
+    in the two slots: the key tiles the two need differ (a key tile fully masked for one query
+    tile only), the last pair of an odd tile count has no second tile, rows with no kept key
+    give lse = -inf and O = 0; O, lse and the gradients match the oracle.  (Nk is a multiple
+    of 8: dense mask and bias rows must start on 16-byte boundaries.)"""
+    g = torch.Generator().manual_seed(7000 + d + 10 * Hq + Nq)
+    B = 2
+    inp = dict(q=torch.randn(B, Nq, Hq, d, generator=g).bfloat16(), k=torch.randn(B, Nk, Hkv, d, generator=g).bfloat16(),
+               v=torch.randn(B, Nk, Hkv, d, generator=g).bfloat16(), dout=torch.randn(B, Nq, Hq, d, generator=g).bfloat16())
+    keep = torch.rand(B, Hkv, Nq, Nk, generator=g) < 0.5
+    keep[:, :, 0:128, 128:256] = False           # key tile 1: skipped by query tile 0 only
+    keep[:, :, 128:256, 0:128] = False           # key tile 0: skipped by query tile 1 only
+    keep[:, :, 130:140] = False                  # rows with no kept key
+    keep[0, :, :, 256:] = True                   # full tiles (ragged in k) on batch 0
+    inp["mask"] = keep.bfloat16()
+    if with_bias:
+        inp["bias"] = torch.randn(B, Hkv, Nq, Nk, generator=g).bfloat16()
+    run_and_compare(F, inp, causal, 1.0 / math.sqrt(d), case=f"pairs d{d} hq{Hq} hkv{Hkv} nq{Nq} nk{Nk}")
+
+
 def test_one_head_per_kv_head_with_bias(F):
     """G = 1 with a bias: the backward keeps one dO slot and reloads the bias buffer after each
     query tile's bias copy (no second dO slot to alternate with)."""
@@ -496,7 +521,7 @@ def test_bounded_wait_unwind(F, variant):
         wl = W.scaled(W.WORKLOADS["n4096_hq32_hkv8"], Nq=512, Nk=512, Hq=4, Hkv=2, keep_window=200, seed=91)
         inp = W.make_inputs(wl)
         causal, scale = True, wl.scale
-    elif variant == "colranges_g3":  # single-head forward (odd group), backward without bias
+    elif variant == "colranges_g3":  # paired-query-tile forward (odd group), backward without bias
         wl = W.Workload("doc_unwind", 1, 384, 384, 3, 1, 64, True, 0.125, "colranges", 0, False, doc_lo=50,
                         doc_hi=200, seed=92)
         inp = W.make_inputs(wl)
