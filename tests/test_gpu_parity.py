@@ -508,7 +508,7 @@ def test_one_head_per_kv_head_with_bias(F):
     run_and_compare(F, inp, True, wl.scale)
 
 
-@pytest.mark.parametrize("variant", ["bias_g2", "colranges_g3", "wide256_bias", "wide192_colranges"])
+@pytest.mark.parametrize("variant", ["bias_g2", "colranges_g3", "bias_g1", "wide256_bias", "wide192_colranges"])
 def test_bounded_wait_unwind(F, variant):
     """FDMA_FLAG_TEST_SHORT_WAIT makes the softmax / compute warps' first wait expire (a
     barrier nothing arrives at, ~100 us limit): forward and backward report
@@ -519,6 +519,10 @@ def test_bounded_wait_unwind(F, variant):
     T = F.FDMA_FLAG_TEST_SHORT_WAIT
     if variant == "bias_g2":  # two-head forward, backward with bias and dBias
         wl = W.scaled(W.WORKLOADS["n4096_hq32_hkv8"], Nq=512, Nk=512, Hq=4, Hkv=2, keep_window=200, seed=91)
+        inp = W.make_inputs(wl)
+        causal, scale = True, wl.scale
+    elif variant == "bias_g1":  # paired-query-tile forward with per-slot bias buffers, backward at G = 1
+        wl = W.scaled(W.WORKLOADS["n4096_hq32_hkv8"], Nq=392, Nk=392, Hq=2, Hkv=2, keep_window=150, seed=96)
         inp = W.make_inputs(wl)
         causal, scale = True, wl.scale
     elif variant == "colranges_g3":  # paired-query-tile forward (odd group), backward without bias
@@ -554,7 +558,7 @@ def test_bounded_wait_unwind(F, variant):
     run_and_compare(F, inp, causal, scale)
 
 
-@pytest.mark.parametrize("d,Hq,Hkv", [(64, 6, 2), (64, 8, 2), (64, 4, 2), (128, 8, 2)])
+@pytest.mark.parametrize("d,Hq,Hkv", [(64, 6, 2), (64, 8, 2), (64, 4, 2), (128, 8, 2), (64, 2, 2), (128, 3, 3)])
 def test_backward_repeatable(F, d, Hq, Hkv):
     """dK, dV and dBias are bit for bit the same over repeated calls (dQ is summed by atomics in
     an order that varies).  With a bias the compute threads read the bias buffer with ordinary
