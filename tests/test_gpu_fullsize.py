@@ -3,7 +3,9 @@ times (classify, then forward and backward reusing the classification).
 
 N=4096 is compared element by element.  At N=16384, N=65536 and the
 document-mask workload the oracle recomputes sampled query rows one by one
-(O, lse, dQ for every head of the group, dBias, block-map rows, bit-exact).
+(O, lse, dQ for every head of the group, dBias, block-map rows, bit-exact);
+the same recipe at N = 15896 with odd group sizes and MHA (the forward's paired
+query tiles, an odd tile count and a ragged tail) is checked the same way.
 dK and dV are compared element by element on the whole of kv group 0 at
 N=16384, and at N=65536 and on the document mask on the last 256 key columns of
 one kv group: under the causal mask (and, for the document mask, inside the key's
@@ -227,3 +229,22 @@ def test_docmask_sampled_rows(F):
     check_dk_dv_identities(p, wl, lse, dk, dv, inp["dout"])
     # document masks skip most tiles
     assert (bm.cpu().numpy() == 0).mean() > 0.8
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(6, 2), (3, 3)])
+def test_odd_groups_sampled_rows(F, Hq, Hkv):
+    """Odd group sizes and MHA at full length on the bench recipe (causal top-2048 with a bias),
+    N = 15896: the forward pairs the query tiles of one head (125 tiles, so the last pair has no
+    second tile; a ragged tail of 24 rows).  Sampled rows (O, lse, dQ, dBias, block-map rows),
+    dK / dV of the last 256 keys element by element, and the identities."""
+    wl = W.scaled(W.WORKLOADS["n16384_hq16_hkv4"], Nq=15896, Nk=15896, Hq=Hq, Hkv=Hkv, seed=1010 + Hq)
+    inp = W.make_inputs(wl, device="cuda")
+    bm, out, lse, dq, dk, dv, db = run_bench_config(F, wl, inp)
+    p = orc.Problem(inp["q"], inp["k"], inp["v"], bias=inp["bias"], mask=inp["mask"], causal=True,
+                    scale=wl.scale, dout=inp["dout"])
+    case = f"N=15896 Hq{Hq} Hkv{Hkv} (sampled rows; dK/dV of the last 256 keys element-wise)"
+    rows = sample_rows(wl.Nq, 10, 40 + Hq) + [wl.Nq - 24, wl.Nq - 25, 124 * 128 - 1]
+    record(case, **check_rows(p, wl, bm, out, lse, dq, db, 0, Hkv - 1, sorted(set(rows))))
+    ek, ev = check_last_key_columns(p, wl, dk, dv, 0, Hkv - 1)
+    record(case, dk_rel_l2=ek, dv_rel_l2=ev)
+    check_dk_dv_identities(p, wl, lse, dk, dv, inp["dout"])
