@@ -809,7 +809,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // leave the SM about as fast as the memory system accepts them: a backlog of
           // reductions stalls the other warps' shared-memory and TMEM accesses and the tensor
           // core's operand reads.
-          if (row < p.d) {  // head-dim rows past d are padding (zero)
+          // Head-dim rows past d are padding: a warp whose 32 rows all lie past d skips, the
+          // others add all their rows (those past d hold zeros, as K's padded columns are
+          // zero-filled; they land in the accumulator's padding).  A warp with only some lanes
+          // active made the whole backward about 25 % slower at d = 80 or 112.
+          if (quad * 32 < p.d) {
             float* dst = p.dq_acc + dq_acc_index(b, h, q0, row, p.Hq, p.nqpad, 128);
 #pragma unroll
             for (int u = 0; u < 8; ++u)
