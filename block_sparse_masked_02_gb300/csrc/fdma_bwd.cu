@@ -117,38 +117,25 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
   for (int64_t k = z0 + threadIdx.x; k < z1; k += blockDim.x) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// 64-wide accumulator (B, Hq, 16, nqpad, 4) -> bf16 dQ: one thread per (query, 8 head-dim
-// columns), consecutive threads on consecutive queries, so a warp's two 16-byte loads read
-// contiguous bytes; each thread stores its 8 columns as 16 bytes.
-__global__ void __launch_bounds__(256) dq_convert64_kernel(const DqConvertParams p) {
+// Accumulator grouped by four head-dim columns, (B, Hq, dpad/4, nqpad, 4) (64-wide kernels and
+// the wide head dims) -> bf16 dQ: one thread per (query, 8 head-dim columns), consecutive
+// threads on consecutive queries, so a warp's two 16-byte loads read contiguous bytes; each
+// thread stores its 8 columns as 16 bytes.
+__global__ void __launch_bounds__(256) dq_convert_grouped_kernel(const DqConvertParams p) {
+  const int groups8 = p.dpad >> 3;
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
-  const int64_t total = static_cast<int64_t>(p.B) * p.Hq * 8 * p.nqpad;
+  const int64_t total = static_cast<int64_t>(p.B) * p.Hq * groups8 * p.nqpad;
   if (idx >= total) return;
   const int i = static_cast<int>(idx % p.nqpad);
   const int64_t rest = idx / p.nqpad;
-  const int c8 = static_cast<int>(rest % 8);
-  const int64_t bh = rest / 8;
+  const int c8 = static_cast<int>(rest % groups8);
+  const int64_t bh = rest / groups8;
   if (i >= p.Nq || c8 * 8 >= p.d) return;
   const int h = static_cast<int>(bh % p.Hq), b = static_cast<int>(bh / p.Hq);
-  const float* src = p.dq_acc + ((bh * 16 + 2 * c8) * p.nqpad + i) * 4;
+  const float* src = p.dq_acc + ((bh * (p.dpad >> 2) + 2 * c8) * p.nqpad + i) * 4;
   const float4 a = *reinterpret_cast<const float4*>(src);
   const float4 c = *reinterpret_cast<const float4*>(src + static_cast<int64_t>(p.nqpad) * 4);
   *reinterpret_cast<uint4*>(p.dq + ((static_cast<int64_t>(b) * p.Nq + i) * p.Hq + h) * p.d + c8 * 8) =
-      make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(c.x, c.y), pack_bf16x2(c.z, c.w));
-}
-
-// Wide head dims' accumulator (B, nqpad, Hq, dpad): one thread per 8 consecutive dQ elements.
-__global__ void __launch_bounds__(256) dq_convert_kernel(const DqConvertParams p) {
-  const int64_t idx = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 8;  // element of (b, i, h, d)
-  const int64_t total = static_cast<int64_t>(p.B) * p.Nq * p.Hq * p.d;
-  if (idx >= total) return;
-  const int64_t per_b = static_cast<int64_t>(p.Nq) * p.Hq * p.d;
-  const int64_t b = idx / per_b, rest = idx % per_b;
-  const int64_t row = rest / p.d, col = rest % p.d;  // (i, h) and head-dim column (8 per thread)
-  const float* src = p.dq_acc + (b * static_cast<int64_t>(p.nqpad) * p.Hq + row) * p.dpad + col;
-  const float4 a = *reinterpret_cast<const float4*>(src);
-  const float4 c = *reinterpret_cast<const float4*>(src + 4);
-  *reinterpret_cast<uint4*>(p.dq + idx) =
       make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(c.x, c.y), pack_bf16x2(c.z, c.w));
 }
 
@@ -921,15 +908,9 @@ cudaError_t launch_dq_convert(const DqConvertParams& p, cudaStream_t stream) {
     dq_convert4_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
     return cudaGetLastError();
   }
-  if (p.dpad == 64) {
-    const int64_t threads = static_cast<int64_t>(p.B) * p.Hq * 8 * p.nqpad;
-    if (threads == 0) return cudaSuccess;
-    dq_convert64_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(p);
-    return cudaGetLastError();
-  }
-  const int64_t total = static_cast<int64_t>(p.B) * p.Nq * p.Hq * p.d / 8;
-  if (total == 0) return cudaSuccess;
-  dq_convert_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(p);
+  const int64_t threads = static_cast<int64_t>(p.B) * p.Hq * (p.dpad >> 3) * p.nqpad;
+  if (threads == 0) return cudaSuccess;
+  dq_convert_grouped_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -581,12 +581,15 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           tc_fence_before();
           mbar_arrive(&bars[wDqFree]);
           if (i < p.Nq) {
+            // the accumulator is grouped by four head-dim columns: a warp's reductions of one
+            // group cover 32 consecutive queries, 512 contiguous bytes
             float* dst = p.dq_acc + dq_acc_index(b, h, i, KC0, p.Hq, p.nqpad, DQK);
+            const int64_t gstep = static_cast<int64_t>(p.nqpad) * 4;  // next group of four columns
 #pragma unroll
             for (int c = 0; c < KW / 32; ++c)
 #pragma unroll
               for (int v = 0; v < 8; ++v)
-                red_add_v4(dst + c * 32 + 4 * v, __uint_as_float(r[c][4 * v]), __uint_as_float(r[c][4 * v + 1]),
+                red_add_v4(dst + (c * 8 + v) * gstep, __uint_as_float(r[c][4 * v]), __uint_as_float(r[c][4 * v + 1]),
                            __uint_as_float(r[c][4 * v + 2]), __uint_as_float(r[c][4 * v + 3]));
           }
         }

@@ -90,15 +90,13 @@ struct BwdPreParams {
 // groups of four query rows, (B, Hq, nqpad/4, 128, 4): element (query i, head-dim c) of a
 // head sits at ((i/4)*128 + c)*4 + i%4, so the four queries of one head-dim index are one
 // 16-byte vector and 32 consecutive head-dim indices are 512 contiguous bytes.  For the
-// 64-wide kernels it is grouped by four head-dim columns, (B, Hq, 16, nqpad, 4): the four
-// columns of one query are one 16-byte vector and 32 consecutive queries are 512 contiguous
-// bytes.  For the wide head dims it is (B, nqpad, Hq, dpad).
+// 64-wide kernels and the wide head dims (a TMEM lane holds a query there) it is grouped by
+// four head-dim columns, (B, Hq, dpad/4, nqpad, 4): the four columns of one query are one
+// 16-byte vector and 32 consecutive queries are 512 contiguous bytes.
 __host__ __device__ inline int64_t dq_acc_index(int b, int h, int i, int c, int Hq, int nqpad, int dpad) {
   if (dpad == 128)
     return (((static_cast<int64_t>(b) * Hq + h) * (nqpad >> 2) + (i >> 2)) * 128 + c) * 4 + (i & 3);
-  if (dpad == 64)
-    return (((static_cast<int64_t>(b) * Hq + h) * 16 + (c >> 2)) * nqpad + i) * 4 + (c & 3);
-  return ((static_cast<int64_t>(b) * nqpad + i) * Hq + h) * dpad + c;
+  return (((static_cast<int64_t>(b) * Hq + h) * (dpad >> 2) + (c >> 2)) * nqpad + i) * 4 + (c & 3);
 }
 
 struct BwdParams {
