@@ -42,7 +42,7 @@ KERNELS_PER_STEP = 5  # classify, fwd, bwd_pre, bwd, dq_convert
 # group of the workload (Hq=4, Hkv=1) is captured; the four kv groups are independent CTAs
 # with the same work, so the full launch moves 4x that: 373,442,048 read and 533,421,056
 # written per kv group.
-BWD_TRAFFIC_BYTES = {"n16384_hq16_hkv4": 4 * (373442048 + 533421056)}
+BWD_TRAFFIC_BYTES = {"n16384_hq16_hkv4": 4 * (373199104 + 532822272)}
 E2E_MAX_HOST_BYTES = 24e9  # larger workloads report no end-to-end number (pinned host copies)
 
 
